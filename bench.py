@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache attention path on one GB300 (or N independent replicas).
+
+A step is one pass of the whole path over the mixed continuous batch (256 decode requests with
+seq_lens ~ U[128, 8192] plus 4 prefill chunks of 512 tokens; H=16, Hk=4, head_dim 128, bf16,
+page 16): the fused RoPE + out_cache_loc cache write over all 2304 new tokens, varlen causal
+prefill over the chunks, then split-K decode with its log-sum-exp merge.
+
+value  = algorithmic bytes of the step (decode K/V + index + q/out, the rotate+write traffic,
+         prefill q/out and K/V read once) / device time of the step (CUDA events, K steps).
+e2e    = the same metric with the step's inputs copied from pinned host memory and its
+         outputs read back inside the timed region.
+roofline: the decode call (partial kernel + merge) against the measured HBM copy bandwidth.
+Every step reads ~2.2 GB of K/V, far more than the 129 MB L2, so no flush is needed.
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores on a bounded
+sample of the same step and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn GB/s (% HBM peak); prefill attn TFLOP/s (% TC peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic work of one step
+# ---------------------------------------------------------------------------------------------
+
+
+def step_work(wl, dec_sel=None, pre_rows=None, rope=True):
+    """Bytes / FLOPs the step must move or compute (each counted once).
+
+    decode: per cached token K+V of every KV head plus its 4-byte slot index; per request q
+            in and decode_out.
+    rope:   per token q,k,v read and q_out,k,v written, position + slot, its freqs row.
+    prefill: q in and out, K/V of every key position read once; FLOPs 4*d*H per unmasked
+            (query, key) pair (QK^T and PV).
+    """
+    pool = wl.pool
+    esz = 2 if pool.dtype == "bf16" else 4
+    H, Hk, D = wl.n_heads, pool.n_kv_heads, pool.head_dim
+    out = {"decode_bytes": 0.0, "rope_bytes": 0.0, "prefill_bytes": 0.0, "prefill_flops": 0.0}
+    if wl.decode is not None:
+        sl = wl.decode.seq_lens if dec_sel is None else wl.decode.seq_lens[dec_sel]
+        out["decode_bytes"] = float(sl.sum()) * (2 * Hk * D * esz + 4) + len(sl) * 2 * H * D * esz
+    if rope and wl.rope is not None:
+        T = wl.rope.n_tokens
+        out["rope_bytes"] = T * (2.0 * (H + 2 * Hk) * D * esz + 8 + 4 * D)
+    if wl.prefill is not None:
+        p = wl.prefill
+        q = (p.qo_indptr[1:] - p.qo_indptr[:-1]).astype("int64")
+        k = (p.kv_indptr[1:] - p.kv_indptr[:-1]).astype("int64")
+        pre = k - q
+        if pre_rows is None:
+            pairs = float((q * pre + q * (q + 1) // 2).sum())
+            nq = float(q.sum())
+            nk = float(k.sum())
+        else:  # a subset of packed rows: each row attends prefix + its index + 1 keys
+            import numpy as np
+            b = np.searchsorted(p.qo_indptr, pre_rows, side="right") - 1
+            i = pre_rows - p.qo_indptr[b]
+            pairs = float((pre[b] + i + 1).sum())
+            nq = float(len(pre_rows))
+            nk = float(k[np.unique(b)].sum())
+        out["prefill_flops"] = 4.0 * D * H * pairs
+        out["prefill_bytes"] = nq * 2 * H * D * esz + nk * 2 * Hk * D * esz
+    out["total_bytes"] = out["decode_bytes"] + out["rope_bytes"] + out["prefill_bytes"]
+    return out
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (replicas: no data-path collective)
+# ---------------------------------------------------------------------------------------------
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+# the CPU oracle as a baseline (test infrastructure, timed as it stands)
+# ---------------------------------------------------------------------------------------------
+
+
+def oracle_sample(wl, dec_fraction=1.0, pre_fraction=1.0):
+    import numpy as np
+    dsel = None
+    prows = None
+    if wl.decode is not None and dec_fraction < 1.0:
+        n = max(1, int(round(wl.decode.batch * dec_fraction)))
+        dsel = np.arange(n, dtype=np.int32)
+    if wl.prefill is not None and pre_fraction < 1.0:
+        tot = wl.prefill.total_q
+        n = max(1, int(round(tot * pre_fraction)))
+        prows = np.linspace(0, tot - 1, n).astype(np.int32)
+    return dsel, prows
+
+
+def run_oracle_step(wl, kl, vl, dsel, prows):
+    import numpy as np
+    import oracle
+    r = wl.rope
+    q = oracle.rope_kv_write(r.q, r.k, r.v, r.freqs_cis, r.position_ids, r.out_cache_loc, kl, vl)
+    if wl.prefill is not None:
+        p = wl.prefill
+        qp = q[p.q_token_offset: p.q_token_offset + p.total_q]
+        oracle.prefill(qp, kl, vl, wl.pool.req_to_token, p.req_pool_indices, p.qo_indptr,
+                       p.kv_indptr, rows=prows)
+    if wl.decode is not None:
+        d = wl.decode
+        qd = np.ascontiguousarray(q[: d.batch])
+        oracle.decode(qd, kl, vl, wl.pool.req_to_token, d.req_pool_indices, d.seq_lens, sel=dsel)
+
+
+def cpu_baseline(wl, dec_fraction, pre_fraction, repeats=1):
+    import numpy as np
+    import oracle
+    oracle.build()
+    kl = np.ascontiguousarray(wl.pool.k_buffer[0]).copy()
+    vl = np.ascontiguousarray(wl.pool.v_buffer[0]).copy()
+    dsel, prows = oracle_sample(wl, dec_fraction, pre_fraction)
+    work = step_work(wl, dsel, prows)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        run_oracle_step(wl, kl, vl, dsel, prows)
+    dt = (time.perf_counter() - t0) / repeats
+    desc = (f"rope+write of all {wl.rope.n_tokens} tokens, prefill of "
+            f"{'all' if prows is None else len(prows)} of {wl.prefill.total_q} rows, decode of "
+            f"{'all' if dsel is None else len(dsel)} of {wl.decode.batch} requests")
+    return {"value": work["total_bytes"] / dt / 1e9, "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+            "seconds_per_sample": dt}
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from paged_kv_cache_apply_gb300 import build as B
+    if rank == 0:
+        B.build()
+    barrier(world)
+    B.build()
+    import paged_kv_cache_apply_gb300 as A
+    from paged_kv_cache_apply_gb300 import device as DV
+    from paged_kv_cache_apply_gb300 import workloads as W
+
+    wl = W.config5()
+    dw = DV.DeviceWorkload.upload(wl)
+    work = step_work(wl)
+    chunk, n_splits = A.astr_decode_plan(dw.decode["kv"], wl.n_heads)
+    launches_per_step = 3 + (1 if n_splits > 1 else 0)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        dw.run_step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        dw.run_rope()
+        ev[i][1].record(stream)
+        dw.run_prefill()
+        ev[i][2].record(stream)
+        dw.run_decode()
+        ev[i][3].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    rope_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    ms_step = max_over_ranks(total_ms / K, world, torch.device("cuda", local))
+
+    # end to end: inputs from pinned host memory, outputs read back, every step
+    h_in = {}
+    r, pz, dz = dw.rope, dw.prefill, dw.decode
+    dev_inputs = [r["q"], r["k"], r["v"], r["pos"], r["loc"],
+                  pz["kv"].req_pool_indices, pz["kv"].qo_indptr, pz["kv"].kv_indptr,
+                  pz["kv"].q_tile_to_batch, pz["kv"].q_tile_to_index,
+                  dz["kv"].req_pool_indices, dz["kv"].seq_lens, dz["kv"].kv_indptr]
+    for i, t in enumerate(dev_inputs):
+        h_in[i] = t.to("cpu").pin_memory()
+    h_out = [torch.empty_like(pz["out"], device="cpu").pin_memory(),
+             torch.empty_like(dz["out"], device="cpu").pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in dev_inputs)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for i, t in enumerate(dev_inputs):
+            t.copy_(h_in[i], non_blocking=True)
+        dw.run_step()
+        h_out[0].copy_(pz["out"], non_blocking=True)
+        h_out[1].copy_(dz["out"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, torch.device("cuda", local))
+
+    peaks, peak_kind = read_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    dec_gbs = work["decode_bytes"] / (dec_ms * 1e-3) / 1e9
+    rope_gbs = work["rope_bytes"] / (rope_ms * 1e-3) / 1e9
+    pre_tflops = work["prefill_flops"] / (pre_ms * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                td = json.load(f)
+            if td.get("kernel_source_sha") == _decode_source_sha():
+                traffic = td.get("dram_bytes_per_launch_full_size")
+        except Exception:
+            traffic = None
+
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC,
+        "value": round(world * work["total_bytes"] / (ms_step * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "mixed continuous batch: 256 decode requests seq_lens~U[128,8192] + 4 "
+                        "prefill chunks x 512 tokens, fused rope+out_cache_loc write of 2304 "
+                        "tokens; n_heads 16, n_kv_heads 4, head_dim 128, bf16, page 16, "
+                        "freqs max_len 8192",
+            "l2": "no flush: each step reads ~2.2 GB of K/V (> 129 MB L2)",
+            "parallelism": f"replicas x{world}",
+            "decode_split_chunk": chunk, "decode_splits": n_splits,
+        },
+        "rows": {
+            "rope_kv_write": {"ms": round(rope_ms, 5), "GB/s": round(rope_gbs, 1),
+                              "frac_hbm": round(rope_gbs / hbm, 4)},
+            "prefill": {"ms": round(pre_ms, 5), "TFLOP/s": round(pre_tflops, 2),
+                        "frac_tc": round(pre_tflops / tc, 4)},
+            "decode": {"ms": round(dec_ms, 5), "GB/s": round(dec_gbs, 1),
+                       "frac_hbm": round(dec_gbs / hbm, 4)},
+        },
+        "roofline": {"kernel": "astr_decode_attention (partial + merge)", "bound": "hbm",
+                     "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(dec_gbs / hbm, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (hbm_gbs)"},
+        "e2e": {"value": round(world * work["total_bytes"] / (e2e_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(K * launches_per_step),
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, 1.0, 1.0)
+    print(json.dumps(out), flush=True)
+
+
+def _decode_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ["simt_attention.cu", "astr_internal.cuh"]:
+        with open(os.path.join(ROOT, "paged_kv_cache_apply_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------------------------
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_kv_cache_apply_gb300 import workloads as W
+    import numpy as np
+    import oracle
+    oracle.build()
+    wl = W.config5()
+    kl = np.ascontiguousarray(wl.pool.k_buffer[0]).copy()
+    vl = np.ascontiguousarray(wl.pool.v_buffer[0]).copy()
+    dsel, prows = oracle_sample(wl, 1.0 / 16, 1.0 / 16)
+    work = step_work(wl, dsel, prows)
+    for _ in range(args.warmup):
+        run_oracle_step(wl, kl, vl, dsel, prows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(wl, kl, vl, dsel, prows)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = work["total_bytes"] / dt / 1e9
+    sample = (f"per step: rope+write of all {wl.rope.n_tokens} tokens, prefill of {len(prows)} of "
+              f"{wl.prefill.total_q} rows, decode of {len(dsel)} of {wl.decode.batch} requests")
+    out = {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "mixed continuous batch (same as the GPU arm), bounded sample",
+                      "parallelism": "host cores (OpenMP)"},
+           "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * astr.h -- C ABI of libastr.so, the GB300 (sm_103a) paged KV-cache attention path.
+ *
+ * The path: RoPE applied to Q/K from a precomputed f32 [cos, sin] table and written into the
+ * KV cache at out_cache_loc (rotation before the write), then GQA softmax(q.k/sqrt(d)).v over
+ * a paged k_buffer / v_buffer, for decode (split-K partials merged by log-sum-exp) and for
+ * varlen causal prefill (including prefill resumed after a cached prefix).
+ *
+ * Sources: the AstrAI documentation -- internals page ("Autoregression & Causal Masking",
+ * "Rotary Position Embedding (RoPE)", "KV Cache Mathematics", "Cache Architecture",
+ * "Attention Backend") and inference guide ("KV Cache", "KVCache System", "Attention
+ * Backend", "Rotary Embedding Backend").
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer inside astr_kv_cache and every tensor argument is a DEVICE pointer owned by
+ *    the caller. The library allocates nothing and frees nothing; it writes only the outputs
+ *    named at each call (and, for decode, the caller's split-K scratch).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t / CUstream handle; NULL is
+ *    the legacy default stream). No call synchronises the host unless checked mode is on.
+ *  - Layouts are row-major and packed: q/k/v rows are [token, head, head_dim] (the pages'
+ *    blhd layout with batch and sequence flattened), the cache is
+ *    [n_layers, size, n_kv_heads, head_dim], index arrays are int32.
+ *  - Element types: ASTR_F32 or ASTR_BF16 for q, k, v, the cache and the outputs; freqs_cis
+ *    is always f32. head_dim is 64 or 128. n_heads must be a multiple of n_kv_heads (GQA:
+ *    query head h reads KV head h / (n_heads / n_kv_heads)).
+ *  - The softmax scale is always 1/sqrt(head_dim) (internals page, "Attention Backend").
+ *  - Errors: arguments are validated on the host before any launch; a failure returns
+ *    ASTR_ERR_INVALID / ASTR_ERR_UNSUPPORTED, enqueues nothing and sets astr_last_error().
+ *    Kernels bounds-check every gathered slot, position and page-table row; an out-of-range
+ *    index skips that access and raises a bit in a per-device error word instead of faulting.
+ *    Every wait inside a kernel is bounded in time; a wait that runs out raises
+ *    ASTR_DEVERR_TIMEOUT. astr_device_error() reads and clears the word. Nothing ever falls
+ *    back to another implementation.
+ */
+#ifndef ASTR_H_
+#define ASTR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *astr_stream; /* cudaStream_t */
+
+typedef enum { ASTR_F32 = 0, ASTR_BF16 = 1 } astr_dtype;
+
+typedef enum {
+  ASTR_OK = 0,
+  ASTR_ERR_INVALID = 1,     /* bad argument: null pointer, inconsistent sizes */
+  ASTR_ERR_UNSUPPORTED = 2, /* valid but not implemented: head_dim, dtype, group size */
+  ASTR_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  ASTR_ERR_INDEX = 4,       /* checked mode: a kernel met an out-of-range index */
+  ASTR_ERR_TIMEOUT = 5      /* checked mode: a kernel wait ran out of time */
+} astr_status;
+
+/* bits of the per-device error word */
+#define ASTR_DEVERR_SLOT 0x1u     /* a slot outside [0, size) */
+#define ASTR_DEVERR_POS 0x2u      /* a position outside [0, freqs_max_len) */
+#define ASTR_DEVERR_ROW 0x4u      /* a req_pool_indices entry outside [0, num_reqs) */
+#define ASTR_DEVERR_LEN 0x8u      /* a length < 1 or beyond max_ctx_len / max_len */
+#define ASTR_DEVERR_TIMEOUT 0x10u /* a bounded wait ran out */
+#define ASTR_DEVERR_META 0x20u    /* checked mode: indptr / tile map inconsistent */
+
+/*
+ * The pages' KVCache dataclass (inference guide, "KVCache System": "pure data, no methods"),
+ * as plain device pointers and host sizes. Fields a call does not use may be NULL / 0.
+ */
+typedef struct astr_kv_cache {
+  /* KVStorage: flat token-level buffers [n_layers, size, n_kv_heads, head_dim] of `dtype` */
+  void *k_buffer;
+  void *v_buffer;
+  int32_t n_layers;
+  int32_t n_kv_heads;
+  int64_t size;
+  int32_t head_dim;
+  int32_t dtype; /* astr_dtype */
+  /* ReqToTokenPool: [num_reqs, max_ctx_len] -> physical slot, shared across layers */
+  const int32_t *req_to_token;
+  int32_t num_reqs;
+  int32_t max_ctx_len;
+  /* the batch of this forward */
+  const int32_t *req_pool_indices; /* [batch] row of req_to_token per request */
+  const int32_t *seq_lens;         /* [batch] decode: cached positions incl. the new token */
+  int32_t batch;
+  int32_t max_len;                 /* host int: max(seq_lens) (decode grid sizing, no sync) */
+  const int32_t *out_cache_loc;    /* [n_tokens] write slots of this forward */
+  int64_t n_tokens;
+  const int32_t *kv_indptr;        /* [batch+1] prefix sum of kv lengths */
+  const int32_t *qo_indptr;        /* [batch+1] prefix sum of q lengths (prefill) */
+  const int32_t *q_tile_to_batch;  /* [num_q_tiles] prefill: tile -> request */
+  const int32_t *q_tile_to_index;  /* [num_q_tiles] prefill: tile -> request-local tile index */
+  int32_t num_q_tiles;
+  int32_t q_tile_rows;             /* rows per Q tile; 128 */
+  /* decode split-K scratch (caller-owned, f32): see astr_decode_attention */
+  float *decode_o_part;            /* [batch, n_heads, max_splits, head_dim] */
+  float *decode_ml_part;           /* [batch, n_heads, max_splits, 2] = (m, l) */
+  int32_t max_splits;
+  int32_t split_chunk;             /* tokens per split; 0 = chosen by the library */
+  void *decode_out;                /* [batch, n_heads, head_dim] of `dtype` */
+} astr_kv_cache;
+
+/*
+ * Fused RoPE + KV cache write (internals page, "Rotary Position Embedding (RoPE)" and "KV
+ * Cache Mathematics": RoPE is applied before the cache write; inference guide, "KVCache
+ * System": k_buffer[layer_id, out_cache_loc] = k; "Rotary Embedding Backend": freqs_cis
+ * [max_len, dim/2, 2] f32, view_as_complex pairing of adjacent elements).
+ *
+ * For every token t < kv->n_tokens with p = position_ids[t], s = kv->out_cache_loc[t] and
+ * (c_i, s_i) = freqs_cis[p, i]:
+ *   q_out[t, h, 2i], q_out[t, h, 2i+1] = rotation of (q[t,h,2i], q[t,h,2i+1]) by (c_i, s_i)
+ *   k_buffer[layer_id, s, g, :]         = the same rotation of k[t, g, :]
+ *   v_buffer[layer_id, s, g, :]         = v[t, g, :]
+ * The rotation is a' = RN(RN(a c) - RN(b s)), b' = RN(RN(a s) + RN(b c)) in f32 with no fused
+ * multiply-add, then rounded to the element type (bf16: nearest, ties to even), so results
+ * are bit-reproducible. q: [n_tokens, n_heads, head_dim]; q_out may equal q (in place);
+ * k, v: [n_tokens, n_kv_heads, head_dim]. Slots in out_cache_loc must be distinct (the
+ * allocator hands out unique slots); duplicates give an unspecified one of the rows. A token
+ * whose position or slot is out of range is skipped (ASTR_DEVERR_POS / _SLOT).
+ */
+astr_status astr_rope_kv_write(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                               void *q_out, const void *k, const void *v, int32_t n_heads,
+                               const float *freqs_cis, int32_t freqs_max_len,
+                               const int32_t *position_ids, astr_stream stream);
+
+/*
+ * Paged GQA decode attention (internals page, "KV Cache Mathematics":
+ * o_n = sum_j softmax(q_n k_j / sqrt(d_k)) v_j; inference guide, "Attention Backend": the
+ * req_to_token table serves as the page table; "KVCache System": decode_o_part /
+ * decode_ml_part split-K partials merged into decode_out).
+ *
+ * For request b < kv->batch with L = seq_lens[b] (1 <= L <= max_len <= max_ctx_len) and row
+ * r = req_pool_indices[b]:
+ *   decode_out[b, h, :] = sum_{j<L} softmax_j(q[b,h,:] . K_j / sqrt(d)) V_j,
+ *   K_j = k_buffer[layer_id, req_to_token[r, j], h / G, :] (V likewise).
+ * The query is the request's newest token (position L-1), whose K/V must already be written.
+ * q: [batch, n_heads, head_dim]. The positions of each request are cut into chunks of C
+ * tokens (C = split_chunk, or chosen by the library when 0; astr_decode_plan reports it).
+ * A request with more than one chunk writes, per chunk s, the normalised partial output to
+ * decode_o_part[b, h, s, :] and (m_s, l_s) to decode_ml_part[b, h, s, :] -- m_s a reference
+ * score (q.k/sqrt(d) units, natural exponent) and l_s = sum_j exp(score_j - m_s) over the
+ * chunk -- and a second kernel merges them by log-sum-exp. Requires
+ * ceil(max_len / C) <= max_splits; the scratch may be NULL only when every request fits in
+ * one chunk (C >= max_len). kv_indptr is not read (checked mode verifies it equals the prefix
+ * sum of seq_lens).
+ */
+astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                                  int32_t n_heads, astr_stream stream);
+
+/*
+ * The split plan astr_decode_attention would use for `kv`: chunk length and the number of
+ * splits ceil(max_len / chunk). Host-only; enqueues nothing.
+ */
+astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *split_chunk,
+                             int32_t *n_splits);
+
+/*
+ * Varlen causal prefill over the paged pool (inference guide, "Attention Backend": a
+ * ragged-batch prefill that reads K/V straight from the flat pool through req_to_token,
+ * addressing each request through qo_indptr and kv_indptr; "KVCache System": q_tile_to_batch
+ * / q_tile_to_index, and prefill resumed right after a cached prefix; internals page,
+ * "Autoregression & Causal Masking").
+ *
+ * Request b owns packed rows qo_indptr[b] .. qo_indptr[b+1]-1 of q and out
+ * ([sum q, n_heads, head_dim]) and keys 0..K_b-1, K_b = kv_indptr[b+1] - kv_indptr[b] >= Q_b.
+ * Row i of request b sits at absolute position P_b + i, P_b = K_b - Q_b (the cached prefix),
+ * and attends keys j <= P_b + i:
+ *   out[t, h, :] = sum_{j <= P_b+i} softmax_j(q[t,h,:] . K_j / sqrt(d)) V_j.
+ * The new tokens' K/V (positions P_b..K_b-1) must already be in the cache. Tile t covers
+ * request q_tile_to_batch[t], rows [q_tile_rows * q_tile_to_index[t], +q_tile_rows) clipped
+ * to Q_b; together the tiles must cover every row exactly once. Rows are written only by
+ * their tile. bf16 runs on the tcgen05 tensor cores (bf16 operands, f32 accumulation);
+ * f32 runs on the CUDA cores in f32 (no TF32).
+ */
+astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                                   void *out, int32_t n_heads, astr_stream stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char *astr_last_error(void);
+
+/*
+ * Checked mode (process-wide, off by default): every entry point also validates the index
+ * metadata on the device, synchronises `stream` after its kernels and returns ASTR_ERR_INDEX
+ * or ASTR_ERR_TIMEOUT when the device error word is set (then clears it).
+ */
+astr_status astr_set_checked(int32_t on);
+
+/*
+ * Upper bound, in nanoseconds, on any single wait inside a kernel (default 1e9). A wait that
+ * runs out abandons the rest of that block's work, raises ASTR_DEVERR_TIMEOUT and returns
+ * after its in-flight copies land. Values below 1 are clamped to 1.
+ */
+astr_status astr_set_wait_timeout_ns(int64_t ns);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's error word (ASTR_DEVERR_*
+ * bits) into *flags.
+ */
+astr_status astr_device_error(astr_stream stream, uint32_t *flags);
+
+/*
+ * Self-test of the bounded-wait path: launches one block that waits on an mbarrier no thread
+ * ever arrives at, with the wait limited to `ns` nanoseconds, then synchronises `stream`.
+ * Returns ASTR_ERR_TIMEOUT (and clears the error word) when the wait ran out as it must; any
+ * other status means the mechanism is broken. The GPU context stays usable afterwards.
+ */
+astr_status astr_selftest_wait_timeout(astr_stream stream, int64_t ns);
+
+/* ABI version of this header (major * 100 + minor). */
+int32_t astr_version(void);
+
+/* sizeof(astr_kv_cache) as compiled into the library (lets bindings check their mirror). */
+int32_t astr_kv_cache_bytes(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASTR_H_ */

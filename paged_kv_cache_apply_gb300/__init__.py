@@ -1,0 +1,242 @@
+"""Python binding of libastr.so: the GB300 paged KV-cache attention path.
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels. The
+names and arguments are those of include/astr.h; torch tensors are passed by data_ptr() after
+device, dtype and contiguity checks, and the stream defaults to torch's current stream. A
+missing library raises at import of the first call -- there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libastr.so")
+
+ASTR_F32, ASTR_BF16 = 0, 1
+STATUS = {0: "ASTR_OK", 1: "ASTR_ERR_INVALID", 2: "ASTR_ERR_UNSUPPORTED", 3: "ASTR_ERR_CUDA",
+          4: "ASTR_ERR_INDEX", 5: "ASTR_ERR_TIMEOUT"}
+DEVERR_SLOT, DEVERR_POS, DEVERR_ROW, DEVERR_LEN, DEVERR_TIMEOUT, DEVERR_META = 1, 2, 4, 8, 16, 32
+
+
+class AstrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class astr_kv_cache(C.Structure):
+    """ctypes mirror of ``astr_kv_cache`` (field order and types as in include/astr.h)."""
+
+    _fields_ = [
+        ("k_buffer", C.c_void_p), ("v_buffer", C.c_void_p),
+        ("n_layers", C.c_int32), ("n_kv_heads", C.c_int32), ("size", C.c_int64),
+        ("head_dim", C.c_int32), ("dtype", C.c_int32),
+        ("req_to_token", C.c_void_p), ("num_reqs", C.c_int32), ("max_ctx_len", C.c_int32),
+        ("req_pool_indices", C.c_void_p), ("seq_lens", C.c_void_p),
+        ("batch", C.c_int32), ("max_len", C.c_int32),
+        ("out_cache_loc", C.c_void_p), ("n_tokens", C.c_int64),
+        ("kv_indptr", C.c_void_p), ("qo_indptr", C.c_void_p),
+        ("q_tile_to_batch", C.c_void_p), ("q_tile_to_index", C.c_void_p),
+        ("num_q_tiles", C.c_int32), ("q_tile_rows", C.c_int32),
+        ("decode_o_part", C.c_void_p), ("decode_ml_part", C.c_void_p),
+        ("max_splits", C.c_int32), ("split_chunk", C.c_int32),
+        ("decode_out", C.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load libastr.so (built by ``paged_kv_cache_apply_gb300.build``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m paged_kv_cache_apply_gb300.build` (nvcc, sm_103a)")
+            L = C.CDLL(LIB_PATH)
+            P, I32, I64 = C.c_void_p, C.c_int32, C.c_int64
+            KV = C.POINTER(astr_kv_cache)
+            L.astr_rope_kv_write.argtypes = [KV, I32, P, P, P, P, I32, P, I32, P, P]
+            L.astr_decode_attention.argtypes = [KV, I32, P, I32, P]
+            L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
+            L.astr_prefill_attention.argtypes = [KV, I32, P, P, I32, P]
+            L.astr_last_error.restype = C.c_char_p
+            L.astr_set_checked.argtypes = [I32]
+            L.astr_set_wait_timeout_ns.argtypes = [I64]
+            L.astr_device_error.argtypes = [P, C.POINTER(C.c_uint32)]
+            L.astr_selftest_wait_timeout.argtypes = [P, I64]
+            L.astr_version.restype = I32
+            L.astr_kv_cache_bytes.restype = I32
+            for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
+                         "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
+                         "astr_device_error", "astr_selftest_wait_timeout"]:
+                getattr(L, name).restype = I32
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise AstrError(status, lib().astr_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    """Device pointer of a torch tensor (contiguous), an int, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libastr must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return ASTR_F32
+    if t.dtype == torch.bfloat16:
+        return ASTR_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: libastr takes float32 or bfloat16")
+
+
+@dataclass
+class KVCache:
+    """The pages' ``KVCache`` dataclass over torch device tensors ("pure data, no methods").
+
+    ``k_buffer``/``v_buffer``: [n_layers, size, n_kv_heads, head_dim]; every index tensor is
+    int32. ``max_len`` is a host int. Unused fields stay None.
+    """
+
+    k_buffer: object
+    v_buffer: object
+    req_to_token: object = None
+    req_pool_indices: object = None
+    seq_lens: object = None
+    max_len: int = 0
+    out_cache_loc: object = None
+    kv_indptr: object = None
+    qo_indptr: object = None
+    q_tile_to_batch: object = None
+    q_tile_to_index: object = None
+    q_tile_rows: int = 128
+    decode_o_part: object = None
+    decode_ml_part: object = None
+    split_chunk: int = 0
+    decode_out: object = None
+    batch: Optional[int] = None
+    n_tokens: Optional[int] = None
+
+    def as_c(self) -> astr_kv_cache:
+        import torch
+        kb = self.k_buffer
+        if kb.dim() != 4 or self.v_buffer.shape != kb.shape or self.v_buffer.dtype != kb.dtype:
+            raise ValueError("k_buffer / v_buffer must both be [n_layers, size, n_kv_heads, head_dim]")
+        for name in ["req_to_token", "req_pool_indices", "seq_lens", "out_cache_loc", "kv_indptr",
+                     "qo_indptr", "q_tile_to_batch", "q_tile_to_index"]:
+            t = getattr(self, name)
+            if t is not None and t.dtype != torch.int32:
+                raise TypeError(f"{name} must be int32")
+        c = astr_kv_cache()
+        c.k_buffer, c.v_buffer = _ptr(kb), _ptr(self.v_buffer)
+        c.n_layers, c.size, c.n_kv_heads, c.head_dim = kb.shape[0], kb.shape[1], kb.shape[2], kb.shape[3]
+        c.dtype = _dtype_code(kb)
+        if self.req_to_token is not None:
+            c.req_to_token = _ptr(self.req_to_token)
+            c.num_reqs, c.max_ctx_len = self.req_to_token.shape
+        c.req_pool_indices = _ptr(self.req_pool_indices)
+        c.seq_lens = _ptr(self.seq_lens)
+        if self.batch is not None:
+            c.batch = self.batch
+        elif self.req_pool_indices is not None:
+            c.batch = self.req_pool_indices.shape[0]
+        c.max_len = int(self.max_len)
+        c.out_cache_loc = _ptr(self.out_cache_loc)
+        if self.n_tokens is not None:
+            c.n_tokens = int(self.n_tokens)
+        elif self.out_cache_loc is not None:
+            c.n_tokens = self.out_cache_loc.shape[0]
+        c.kv_indptr = _ptr(self.kv_indptr)
+        c.qo_indptr = _ptr(self.qo_indptr)
+        c.q_tile_to_batch = _ptr(self.q_tile_to_batch)
+        c.q_tile_to_index = _ptr(self.q_tile_to_index)
+        if self.q_tile_to_batch is not None:
+            c.num_q_tiles = self.q_tile_to_batch.shape[0]
+        c.q_tile_rows = int(self.q_tile_rows)
+        c.decode_o_part = _ptr(self.decode_o_part)
+        c.decode_ml_part = _ptr(self.decode_ml_part)
+        if self.decode_o_part is not None:
+            c.max_splits = self.decode_o_part.shape[2]
+        c.split_chunk = int(self.split_chunk)
+        c.decode_out = _ptr(self.decode_out)
+        return c
+
+
+def _kv(kv):
+    return kv if isinstance(kv, astr_kv_cache) else kv.as_c()
+
+
+def astr_rope_kv_write(kv, layer_id, q, q_out, k, v, n_heads, freqs_cis, freqs_max_len,
+                       position_ids, stream=None) -> None:
+    c = _kv(kv)
+    _check(lib().astr_rope_kv_write(C.byref(c), int(layer_id), _ptr(q), _ptr(q_out), _ptr(k),
+                                    _ptr(v), int(n_heads), _ptr(freqs_cis), int(freqs_max_len),
+                                    _ptr(position_ids), _stream(stream)))
+
+
+def astr_decode_attention(kv, layer_id, q, n_heads, stream=None) -> None:
+    c = _kv(kv)
+    _check(lib().astr_decode_attention(C.byref(c), int(layer_id), _ptr(q), int(n_heads),
+                                       _stream(stream)))
+
+
+def astr_decode_plan(kv, n_heads):
+    c = _kv(kv)
+    chunk, n = C.c_int32(0), C.c_int32(0)
+    _check(lib().astr_decode_plan(C.byref(c), int(n_heads), C.byref(chunk), C.byref(n)))
+    return chunk.value, n.value
+
+
+def astr_prefill_attention(kv, layer_id, q, out, n_heads, stream=None) -> None:
+    c = _kv(kv)
+    _check(lib().astr_prefill_attention(C.byref(c), int(layer_id), _ptr(q), _ptr(out),
+                                        int(n_heads), _stream(stream)))
+
+
+def astr_set_checked(on: bool) -> None:
+    _check(lib().astr_set_checked(1 if on else 0))
+
+
+def astr_set_wait_timeout_ns(ns: int) -> None:
+    _check(lib().astr_set_wait_timeout_ns(int(ns)))
+
+
+def astr_device_error(stream=None) -> int:
+    flags = C.c_uint32(0)
+    _check(lib().astr_device_error(_stream(stream), C.byref(flags)))
+    return flags.value
+
+
+def astr_selftest_wait_timeout(ns: int, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the raw status (ASTR_ERR_TIMEOUT = 5 expected)."""
+    return lib().astr_selftest_wait_timeout(_stream(stream), int(ns))
+
+
+def astr_version() -> int:
+    return lib().astr_version()

@@ -1,0 +1,375 @@
+// extern "C" entry points of libastr.so: host-side validation, split planning, launches,
+// checked mode and the per-device error word. The operations themselves are defined in
+// include/astr.h with the passages of the AstrAI pages they follow.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <string>
+
+#include "astr_internal.cuh"
+#include "launch.h"
+
+namespace astr {
+
+__device__ uint32_t g_error_word = 0;
+
+namespace {
+
+// device address of g_error_word on the current device (looked up once per device)
+uint32_t *error_word() {
+  static uint32_t *cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t *>(p);
+  }
+  return cache[dev];
+}
+
+thread_local std::string t_last_error;
+std::atomic<int> g_checked{0};
+std::atomic<int64_t> g_wait_ns{1000000000LL};
+
+astr_status fail(astr_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+astr_status fail(astr_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+astr_status ok() {
+  t_last_error.clear();
+  return ASTR_OK;
+}
+
+astr_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(ASTR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+astr_status check_cache(const astr_kv_cache *kv, int32_t layer_id, int32_t n_heads) {
+  if (!kv) return fail(ASTR_ERR_INVALID, "kv is NULL");
+  if (!kv->k_buffer || !kv->v_buffer) return fail(ASTR_ERR_INVALID, "k_buffer / v_buffer is NULL");
+  if (!aligned16(kv->k_buffer) || !aligned16(kv->v_buffer))
+    return fail(ASTR_ERR_INVALID, "k_buffer / v_buffer must be 16-byte aligned");
+  if (kv->dtype != ASTR_F32 && kv->dtype != ASTR_BF16)
+    return fail(ASTR_ERR_UNSUPPORTED, "dtype %d is not ASTR_F32 or ASTR_BF16", kv->dtype);
+  if (kv->head_dim != 64 && kv->head_dim != 128)
+    return fail(ASTR_ERR_UNSUPPORTED, "head_dim %d is not 64 or 128", kv->head_dim);
+  if (kv->n_kv_heads < 1) return fail(ASTR_ERR_INVALID, "n_kv_heads %d < 1", kv->n_kv_heads);
+  if (n_heads < 1 || n_heads % kv->n_kv_heads != 0)
+    return fail(ASTR_ERR_INVALID, "n_heads %d is not a positive multiple of n_kv_heads %d", n_heads,
+                kv->n_kv_heads);
+  if (kv->n_layers < 1 || layer_id < 0 || layer_id >= kv->n_layers)
+    return fail(ASTR_ERR_INVALID, "layer_id %d outside [0, %d)", layer_id, kv->n_layers);
+  if (kv->size < 1) return fail(ASTR_ERR_INVALID, "size %lld < 1", (long long)kv->size);
+  return ASTR_OK;
+}
+
+astr_status check_table(const astr_kv_cache *kv) {
+  if (!kv->req_to_token || !kv->req_pool_indices)
+    return fail(ASTR_ERR_INVALID, "req_to_token / req_pool_indices is NULL");
+  if (kv->num_reqs < 1 || kv->max_ctx_len < 1)
+    return fail(ASTR_ERR_INVALID, "req_to_token shape [%d, %d] is empty", kv->num_reqs, kv->max_ctx_len);
+  return ASTR_OK;
+}
+
+// after the launches of one entry point: checked mode synchronises and reads the error word
+astr_status finish(cudaStream_t s) {
+  if (!g_checked.load()) return ok();
+  uint32_t flags = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&flags, g_error_word, sizeof flags, 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "checked mode: reading the device error word");
+  if (flags) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_error_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "checked mode: clearing the device error word");
+    if (flags & ASTR_DEVERR_TIMEOUT)
+      return fail(ASTR_ERR_TIMEOUT, "a kernel wait ran out of time (error word 0x%x)", flags);
+    return fail(ASTR_ERR_INDEX, "a kernel met an out-of-range index (error word 0x%x)", flags);
+  }
+  return ok();
+}
+
+bool use_tc_decode(const astr_kv_cache *kv, int n_heads) {
+  return tc_decode_supported(kv->dtype, kv->head_dim, n_heads / kv->n_kv_heads);
+}
+
+int decode_chunk(const astr_kv_cache *kv, int n_heads) {
+  const int max_len = kv->max_len;
+  if (kv->split_chunk > 0) return kv->split_chunk;
+  if (!kv->decode_o_part || !kv->decode_ml_part || kv->max_splits <= 1) return max_len;
+  const bool tc = use_tc_decode(kv, n_heads);
+  const int tile = tc ? tc_decode_tile_tokens() : simt_tile_tokens(n_heads / kv->n_kv_heads);
+  // Taking the mean length as half of max_len, aim for about eight waves of one resident
+  // block per SM (tensor-core kernel) or four waves of three (CUDA-core kernel); keep the
+  // chunk within [lo, 4096] tokens and never need more splits than the scratch holds.
+  const int64_t est_tokens = (int64_t)kv->batch * max_len / 2;
+  const int64_t target_blocks = (int64_t)num_sms() * (tc ? 8 : 12);
+  int64_t c = est_tokens * kv->n_kv_heads / (target_blocks > 0 ? target_blocks : 1);
+  const int64_t lo = tc ? 512 : 256;
+  if (c < lo) c = lo;
+  if (c > 4096) c = 4096;
+  const int64_t min_c = (max_len + kv->max_splits - 1) / kv->max_splits;
+  if (c < min_c) c = min_c;
+  c = (c + tile - 1) / tile * tile;
+  if (c >= max_len) c = max_len;
+  return (int)c;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------
+// checked-mode metadata validation
+// ------------------------------------------------------------------------------------------
+namespace {
+__global__ void validate_kernel(const astr_kv_cache kv, int what, uint32_t *err) {
+  const int tid = threadIdx.x;
+  if (what == VALIDATE_DECODE) {
+    for (int b = tid; b < kv.batch; b += blockDim.x) {
+      const int L = kv.seq_lens[b];
+      if (L < 1 || L > kv.max_len || L > kv.max_ctx_len) raise_error(err, ASTR_DEVERR_LEN);
+      const int r = kv.req_pool_indices[b];
+      if (r < 0 || r >= kv.num_reqs) raise_error(err, ASTR_DEVERR_ROW);
+      if (kv.kv_indptr && kv.kv_indptr[b + 1] - kv.kv_indptr[b] != L) raise_error(err, ASTR_DEVERR_META);
+    }
+    if (tid == 0 && kv.kv_indptr && kv.kv_indptr[0] != 0) raise_error(err, ASTR_DEVERR_META);
+    return;
+  }
+  // prefill: indptr sanity, every tile inside its request, tile count = sum ceil(Q/rows),
+  // and no two tiles naming the same (request, index)
+  __shared__ long long total;
+  if (tid == 0) total = 0;
+  __syncthreads();
+  long long mine = 0;
+  for (int b = tid; b < kv.batch; b += blockDim.x) {
+    const int Q = kv.qo_indptr[b + 1] - kv.qo_indptr[b];
+    const int K = kv.kv_indptr[b + 1] - kv.kv_indptr[b];
+    if (Q < 0 || K < Q || K > kv.max_ctx_len) raise_error(err, ASTR_DEVERR_LEN);
+    const int r = kv.req_pool_indices[b];
+    if (r < 0 || r >= kv.num_reqs) raise_error(err, ASTR_DEVERR_ROW);
+    if (Q > 0) mine += (Q + kv.q_tile_rows - 1) / kv.q_tile_rows;
+  }
+  atomicAdd(reinterpret_cast<unsigned long long *>(&total), (unsigned long long)mine);
+  __syncthreads();
+  if (tid == 0 && (total != kv.num_q_tiles || kv.qo_indptr[0] != 0 || kv.kv_indptr[0] != 0))
+    raise_error(err, ASTR_DEVERR_META);
+  for (int t = tid; t < kv.num_q_tiles; t += blockDim.x) {
+    const int b = kv.q_tile_to_batch[t], i = kv.q_tile_to_index[t];
+    if (b < 0 || b >= kv.batch) {
+      raise_error(err, ASTR_DEVERR_META);
+      continue;
+    }
+    const int Q = kv.qo_indptr[b + 1] - kv.qo_indptr[b];
+    if (i < 0 || (long long)i * kv.q_tile_rows >= Q) raise_error(err, ASTR_DEVERR_META);
+    for (int u = t + 1; u < kv.num_q_tiles; ++u)
+      if (kv.q_tile_to_batch[u] == b && kv.q_tile_to_index[u] == i) raise_error(err, ASTR_DEVERR_META);
+  }
+}
+}  // namespace
+
+namespace {
+__global__ void selftest_wait_kernel(uint64_t ns, uint32_t *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, ns, err);  // nothing arrives: the wait must run out
+}
+}  // namespace
+
+cudaError_t launch_validate(const astr_kv_cache &kv, int what, uint32_t *err, cudaStream_t stream) {
+  validate_kernel<<<1, 1024, 0, stream>>>(kv, what, err);
+  return cudaGetLastError();
+}
+
+}  // namespace astr
+
+using namespace astr;
+
+extern "C" {
+
+int32_t astr_version(void) { return 100; }
+
+int32_t astr_kv_cache_bytes(void) { return (int32_t)sizeof(astr_kv_cache); }
+
+const char *astr_last_error(void) { return t_last_error.c_str(); }
+
+astr_status astr_set_checked(int32_t on) {
+  g_checked.store(on ? 1 : 0);
+  return ok();
+}
+
+astr_status astr_set_wait_timeout_ns(int64_t ns) {
+  g_wait_ns.store(ns < 1 ? 1 : ns);
+  return ok();
+}
+
+astr_status astr_device_error(astr_stream stream, uint32_t *flags) {
+  if (!flags) return fail(ASTR_ERR_INVALID, "flags is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  const uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_error_word, sizeof v, 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_error_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  *flags = v;
+  return ok();
+}
+
+astr_status astr_selftest_wait_timeout(astr_stream stream, int64_t ns) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t *err = error_word();
+  if (!err) return fail(ASTR_ERR_CUDA, "no CUDA device / error word unavailable");
+  selftest_wait_kernel<<<1, 32, 0, s>>>((uint64_t)(ns < 1 ? 1 : ns), err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  uint32_t flags = 0;
+  const uint32_t zero = 0;
+  e = cudaMemcpyFromSymbolAsync(&flags, g_error_word, sizeof flags, 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbolAsync(g_error_word, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test synchronisation");
+  if (flags & ASTR_DEVERR_TIMEOUT) return fail(ASTR_ERR_TIMEOUT, "the bounded wait ran out (expected)");
+  return ok();
+}
+
+astr_status astr_rope_kv_write(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                               void *q_out, const void *k, const void *v, int32_t n_heads,
+                               const float *freqs_cis, int32_t freqs_max_len,
+                               const int32_t *position_ids, astr_stream stream) {
+  astr_status st = check_cache(kv, layer_id, n_heads);
+  if (st != ASTR_OK) return st;
+  if (kv->n_tokens < 0) return fail(ASTR_ERR_INVALID, "n_tokens %lld < 0", (long long)kv->n_tokens);
+  if (kv->n_tokens == 0) return ok();
+  if (!q || !q_out || !k || !v || !freqs_cis || !position_ids || !kv->out_cache_loc)
+    return fail(ASTR_ERR_INVALID, "q, q_out, k, v, freqs_cis, position_ids and out_cache_loc must be non-NULL");
+  if (!aligned16(q) || !aligned16(q_out) || !aligned16(k) || !aligned16(v) || !aligned16(freqs_cis))
+    return fail(ASTR_ERR_INVALID, "q, q_out, k, v and freqs_cis must be 16-byte aligned");
+  if (freqs_max_len < 1) return fail(ASTR_ERR_INVALID, "freqs_max_len %d < 1", freqs_max_len);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t *err = error_word();
+  if (!err) return fail(ASTR_ERR_CUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = launch_rope_kv_write(*kv, layer_id, q, q_out, k, v, n_heads, freqs_cis,
+                                       freqs_max_len, position_ids, s, num_sms(), err);
+  if (e != cudaSuccess) return cuda_fail(e, "astr_rope_kv_write launch");
+  return finish(s);
+}
+
+astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *split_chunk,
+                             int32_t *n_splits) {
+  if (!kv || !split_chunk || !n_splits) return fail(ASTR_ERR_INVALID, "NULL argument");
+  if (kv->n_kv_heads < 1 || n_heads < 1 || n_heads % kv->n_kv_heads)
+    return fail(ASTR_ERR_INVALID, "n_heads %d / n_kv_heads %d", n_heads, kv->n_kv_heads);
+  if (kv->max_len < 1) return fail(ASTR_ERR_INVALID, "max_len %d < 1", kv->max_len);
+  const int c = decode_chunk(kv, n_heads);
+  *split_chunk = c;
+  *n_splits = (kv->max_len + c - 1) / c;
+  return ok();
+}
+
+astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                                  int32_t n_heads, astr_stream stream) {
+  astr_status st = check_cache(kv, layer_id, n_heads);
+  if (st != ASTR_OK) return st;
+  if (kv->batch < 0) return fail(ASTR_ERR_INVALID, "batch %d < 0", kv->batch);
+  if (kv->batch == 0) return ok();
+  if ((st = check_table(kv)) != ASTR_OK) return st;
+  if (!q || !kv->seq_lens || !kv->decode_out)
+    return fail(ASTR_ERR_INVALID, "q, seq_lens and decode_out must be non-NULL");
+  if (!aligned16(q)) return fail(ASTR_ERR_INVALID, "q must be 16-byte aligned");
+  const int G = n_heads / kv->n_kv_heads;
+  if (!simt_attn_supported(kv->dtype, kv->head_dim, G) && !use_tc_decode(kv, n_heads))
+    return fail(ASTR_ERR_UNSUPPORTED, "decode: group size %d (n_heads / n_kv_heads) not served", G);
+  if (kv->max_len < 1 || kv->max_len > kv->max_ctx_len)
+    return fail(ASTR_ERR_INVALID, "max_len %d outside [1, max_ctx_len %d]", kv->max_len, kv->max_ctx_len);
+  if (kv->split_chunk < 0) return fail(ASTR_ERR_INVALID, "split_chunk %d < 0", kv->split_chunk);
+  SimtAttnPlan plan;
+  plan.mode = 0;
+  plan.chunk = decode_chunk(kv, n_heads);
+  plan.n_splits = (kv->max_len + plan.chunk - 1) / plan.chunk;
+  plan.wait_ns = (uint64_t)g_wait_ns.load();
+  if (plan.n_splits > 1) {
+    if (!kv->decode_o_part || !kv->decode_ml_part)
+      return fail(ASTR_ERR_INVALID, "decode_o_part / decode_ml_part are NULL but %d splits are needed",
+                  plan.n_splits);
+    if (plan.n_splits > kv->max_splits)
+      return fail(ASTR_ERR_INVALID, "max_len %d / split_chunk %d needs %d splits > max_splits %d",
+                  kv->max_len, plan.chunk, plan.n_splits, kv->max_splits);
+  }
+  plan.err = error_word();
+  if (!plan.err) return fail(ASTR_ERR_CUDA, "no CUDA device / error word unavailable");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (g_checked.load() && (e = launch_validate(*kv, VALIDATE_DECODE, plan.err, s)) != cudaSuccess)
+    return cuda_fail(e, "checked-mode validation launch");
+  if (use_tc_decode(kv, n_heads))
+    e = launch_tc_decode(*kv, layer_id, q, n_heads, plan, s);
+  else
+    e = launch_simt_attention(*kv, layer_id, q, kv->decode_out, n_heads, plan, s);
+  if (e != cudaSuccess) return cuda_fail(e, "astr_decode_attention launch");
+  return finish(s);
+}
+
+astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                                   void *out, int32_t n_heads, astr_stream stream) {
+  astr_status st = check_cache(kv, layer_id, n_heads);
+  if (st != ASTR_OK) return st;
+  if (kv->batch < 0 || kv->num_q_tiles < 0) return fail(ASTR_ERR_INVALID, "negative batch / num_q_tiles");
+  if (kv->batch == 0 || kv->num_q_tiles == 0) return ok();
+  if ((st = check_table(kv)) != ASTR_OK) return st;
+  if (!q || !out || !kv->qo_indptr || !kv->kv_indptr || !kv->q_tile_to_batch || !kv->q_tile_to_index)
+    return fail(ASTR_ERR_INVALID, "q, out, qo_indptr, kv_indptr and the q-tile maps must be non-NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(ASTR_ERR_INVALID, "q and out must be 16-byte aligned");
+  if (kv->q_tile_rows != 128) return fail(ASTR_ERR_UNSUPPORTED, "q_tile_rows %d is not 128", kv->q_tile_rows);
+  const int G = n_heads / kv->n_kv_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t *err = error_word();
+  if (!err) return fail(ASTR_ERR_CUDA, "no CUDA device / error word unavailable");
+  cudaError_t e;
+  if (g_checked.load() && (e = launch_validate(*kv, VALIDATE_PREFILL, err, s)) != cudaSuccess)
+    return cuda_fail(e, "checked-mode validation launch");
+  const uint64_t wait_ns = (uint64_t)g_wait_ns.load();
+  if (kv->dtype == ASTR_BF16 && tc_prefill_supported(kv->dtype, kv->head_dim, G, kv->q_tile_rows)) {
+    e = launch_tc_prefill(*kv, layer_id, q, out, n_heads, wait_ns, err, s);
+  } else {
+    if (!simt_attn_supported(kv->dtype, kv->head_dim, G))
+      return fail(ASTR_ERR_UNSUPPORTED, "prefill: group size %d not in {1,2,4,8}", G);
+    SimtAttnPlan plan;
+    plan.mode = 1;
+    plan.chunk = 0;
+    plan.n_splits = 1;
+    plan.wait_ns = wait_ns;
+    plan.err = err;
+    e = launch_simt_attention(*kv, layer_id, q, out, n_heads, plan, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "astr_prefill_attention launch");
+  return finish(s);
+}
+
+}  // extern "C"

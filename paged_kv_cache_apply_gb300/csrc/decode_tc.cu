@@ -1,0 +1,516 @@
+// Paged GQA decode attention on the tcgen05 tensor cores (bf16, head_dim 128).
+//
+// AstrAI internals, "KV Cache Mathematics": o_n = sum_j softmax(q_n k_j / sqrt(d_k)) v_j.
+// AstrAI inference guide, "Attention Backend" (req_to_token as the page table) and "KVCache
+// System" (decode_o_part / decode_ml_part split-K partials, merged by log-sum-exp).
+//
+// Decode reads 512 bytes of K+V per token and KV head and does 4*G multiply-adds per byte,
+// so the block is built around the copy pipeline and keeps the arithmetic off the CUDA
+// cores. One block handles (request, chunk, KV head g) with the G query heads of the group:
+//  * warps 4-7 stream 128-token tiles of this head's K and V slices into a 3-stage ring with
+//    16-byte cp.async copies (two lanes-halves per token row, fully coalesced), writing the
+//    128-byte-swizzled operand layout directly; positions past the chunk are zero-filled;
+//  * warp 8 allocates 64 TMEM columns and issues, per tile, S^T = K Q^T (M = 128 tokens on
+//    the TMEM lanes, N = 16 query rows of which G are the group, K = 128) into one of two
+//    S buffers, and O^T += V^T P^T (M = 128 = head_dim, N = 16, K = 128 tokens) with V read
+//    as an MN-major operand and P^T from shared memory;
+//  * warps 0-3 (one TMEM lane each) read a token's G scores, take the tile max per head
+//    across the 128 lanes (warp shuffles + one named barrier), keep the softmax reference
+//    max lazily (raised only when a score exceeds it by 2^8, then O^T is rescaled in TMEM),
+//    write P^T in bf16 and, after the last tile, normalise O^T and store the output or the
+//    chunk's partial and (m, l).
+// Every wait is bounded; a bad slot is zero-filled and flagged; on a timeout the block stops,
+// waits for its own copies and MMAs, frees TMEM and returns.
+#include <math.h>
+
+#include "astr_internal.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace astr {
+
+namespace {
+
+constexpr int kTok = 128;                 // tokens per tile (M of S^T)
+constexpr int kD = 128;                   // head_dim
+constexpr int kNPad = 16;                 // query rows per MMA (N)
+constexpr int kStages = 3;
+constexpr int kTileBytes = kTok * kD * 2; // 32 KB: K (or V) of one tile
+constexpr int kBlockBytes = kTok * 128;   // 16 KB: one 64-element half of a tile
+constexpr int kThreads = 288;             // 4 softmax + 4 loader + 1 MMA warps
+constexpr float kLazyRescale = 8.0f;
+
+// shared-memory map (offsets from a 1 KB aligned base)
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffQ = kOffV + kStages * kTileBytes;  // 16 rows x 128 -> 2 blocks of 2 KB
+constexpr int kOffP = kOffQ + 4096;                   // 2 buffers x (16 rows x 128 tokens)
+constexpr int kOffRed = kOffP + 2 * 4096;             // [2][4 warps][16] f32 tile maxima
+constexpr int kOffLsum = kOffRed + 2 * 4 * 16 * 4;    // [4 warps][16] f32
+constexpr int kOffBar = kOffLsum + 4 * 16 * 4;
+constexpr int kOffMisc = kOffBar + 32 * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;      // + alignment slack
+
+constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kNPad, false, false);
+constexpr uint32_t kIdescPV = tc::idesc_bf16(128, kNPad, true, false);
+
+struct DecArgs {
+  const void *q;
+  const void *k_layer;
+  const void *v_layer;
+  const int32_t *r2t;
+  const int32_t *rpi;
+  const int32_t *seq_lens;
+  float *o_part;
+  float *ml_part;
+  void *out;
+  int64_t size;
+  uint64_t wait_ns;
+  uint32_t *err;
+  int32_t num_reqs, max_ctx;
+  int32_t H, Hk, B;
+  int32_t chunk, n_splits, max_splits, max_len;
+  float scale_log2;
+};
+
+__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <int G>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&x)[G]) {
+  if constexpr (G <= 4) {
+    uint32_t r[4];
+    tc::tmem_ld4(taddr, r);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < G; ++h) x[h] = __uint_as_float(r[h]);
+  } else if constexpr (G == 8) {
+    uint32_t r[8];
+    tc::tmem_ld8(taddr, r);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < G; ++h) x[h] = __uint_as_float(r[h]);
+  } else {
+    uint32_t r[16];
+    tc::tmem_ld16(taddr, r);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < G; ++h) x[h] = __uint_as_float(r[h]);
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[G]) {
+  if constexpr (G <= 4) {
+    uint32_t r[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int h = 0; h < G; ++h) r[h] = __float_as_uint(x[h]);
+    tc::tmem_st4(taddr, r);
+  } else if constexpr (G == 8) {
+    uint32_t r[8];
+#pragma unroll
+    for (int h = 0; h < G; ++h) r[h] = __float_as_uint(x[h]);
+    tc::tmem_st8(taddr, r);
+  } else {
+    uint32_t r[16];
+#pragma unroll
+    for (int h = 0; h < G; ++h) r[h] = __float_as_uint(x[h]);
+    tc::tmem_st16(taddr, r);
+  }
+  tc::tmem_st_wait();
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *full = bars;                 // [kStages] loaders -> MMA (128 arrivals)
+  uint64_t *empty = bars + kStages;      // [kStages] MMA -> loaders (commit)
+  uint64_t *s_full = bars + 2 * kStages; // [2] MMA -> softmax (commit)
+  uint64_t *p_full = s_full + 2;         // [2] softmax -> MMA (128 arrivals)
+  uint64_t *pv_done = p_full + 2;        // [2] MMA -> softmax (commit)
+  uint64_t *q_full = pv_done + 2;        // softmax -> MMA (128 arrivals)
+  uint64_t *drain = q_full + 1;          // MMA -> itself (commit)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+  float *red = reinterpret_cast<float *>(smem + kOffRed);
+  float *lsum_s = reinterpret_cast<float *>(smem + kOffLsum);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- the work item: (request b, chunk `split`, KV head g) ---------------------------------
+  const int g = blockIdx.x % a.Hk;
+  const int64_t wi = blockIdx.x / a.Hk;
+  const int split = (int)(wi % a.n_splits);
+  const int b = (int)(wi / a.n_splits);
+  const int L = __ldg(a.seq_lens + b);
+  if (L < 1 || L > a.max_len || L > a.max_ctx) {
+    if (split == 0 && g == 0 && tid == 0) raise_error(a.err, ASTR_DEVERR_LEN);
+    return;
+  }
+  const int64_t j0 = (int64_t)split * a.chunk;
+  if (j0 >= L) return;
+  const int64_t j1 = j0 + a.chunk < L ? j0 + a.chunk : L;
+  const int r = __ldg(a.rpi + b);
+  if (r < 0 || r >= a.num_reqs) {
+    if (g == 0 && tid == 0) raise_error(a.err, ASTR_DEVERR_ROW);
+    return;
+  }
+  const int32_t *row = a.r2t + (int64_t)r * a.max_ctx;
+  const int ntiles = (int)((j1 - j0 + kTok - 1) / kTok);
+
+  // ---- set-up --------------------------------------------------------------------------------
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 128);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(q_full, 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(tmem_slot, 64);
+    tc::tmem_relinquish();
+  }
+  if (warp < 4) {  // zero Q and both P buffers (rows past the group stay zero)
+    uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
+    for (int i = tid; i < (4096 + 8192) / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS0 = tmem, tO = tmem + 32;
+
+  if (warp < 4) {
+    // ============================ softmax / epilogue ===========================================
+    {  // the group's query rows into the Q operand (K-major, swizzled)
+      const uint16_t *qh = static_cast<const uint16_t *>(a.q) + ((int64_t)b * a.H + g * G) * kD;
+      for (int k = tid; k < G * 16; k += 128) {
+        const int h = k >> 4, c = k & 15;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(qh + h * kD) + c);
+        *reinterpret_cast<uint4 *>(smem + kOffQ + tc::sw128_chunk_offset(h, c, 2048)) = v;
+      }
+      tc::fence_proxy_async_smem();
+      mbar_arrive(q_full);
+    }
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m[G], l[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+    bool aborted = false;
+    for (int it = 0; it < ntiles; ++it) {
+      const int sb = it & 1;
+      const int64_t tok0 = j0 + (int64_t)it * kTok;
+      const int n = (int)((j1 - tok0) < kTok ? (j1 - tok0) : kTok);
+      bool ok = true;
+      if (it >= 2) ok = mbar_wait(&pv_done[sb], ((it - 2) >> 1) & 1, a.wait_ns, a.err);
+      ok = ok && mbar_wait(&s_full[sb], (it >> 1) & 1, a.wait_ns, a.err);
+      float x[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) x[h] = -INFINITY;
+      if (ok) {
+        tc::fence_after_sync();
+        float s[G];
+        ld_cols<G>(tS0 + lane_base + sb * 16, s);
+        const bool valid = tid < n;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          x[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
+          float wmax = x[h];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+          if (lane == 0) red[(sb * 4 + warp) * 16 + h] = wmax;
+        }
+      }
+      if (bar_any(1, 128, !ok)) {
+        aborted = true;
+        break;
+      }
+      float mnew[G];
+      bool changed = false;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float M = red[(sb * 4 + 0) * 16 + h];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) M = fmaxf(M, red[(sb * 4 + w) * 16 + h]);
+        mnew[h] = (M > m[h] + kLazyRescale) ? M : m[h];
+        changed |= mnew[h] != m[h];
+      }
+      if (changed) {  // the same decision in every thread
+        float alpha[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          alpha[h] = ex2_approx(m[h] - mnew[h]);  // 0 while m is still -inf
+          l[h] *= alpha[h];
+          m[h] = mnew[h];
+        }
+        if (it > 0) {  // O^T holds earlier tiles: rescale it once PV(it-1) has landed
+          const bool ok2 = mbar_wait(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, a.wait_ns, a.err);
+          if (bar_any(1, 128, !ok2)) {
+            aborted = true;
+            break;
+          }
+          tc::fence_after_sync();
+          float o[G];
+          ld_cols<G>(tO + lane_base, o);
+#pragma unroll
+          for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+          st_cols<G>(tO + lane_base, o);
+        }
+      }
+      // P^T for this tile: token `tid` of query row h
+      unsigned char *pb = smem + kOffP + sb * 4096;
+      const int kb = tid >> 6, within = tid & 63;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float p = (tid < n) ? ex2_approx(x[h] - m[h]) : 0.f;
+        l[h] += p;
+        const uint32_t off = (uint32_t)kb * 2048u + (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u +
+                             ((uint32_t)((within >> 3) ^ (h & 7)) << 4) + (uint32_t)(within & 7) * 2u;
+        *reinterpret_cast<uint16_t *>(pb + off) = f32_to_bf16_rn(p);
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      mbar_arrive(&p_full[sb]);
+    }
+
+    if (!aborted && ntiles > 0) {
+      const int last = ntiles - 1;
+      const bool ok = mbar_wait(&pv_done[last & 1], (last >> 1) & 1, a.wait_ns, a.err);
+      if (bar_any(1, 128, !ok)) {
+        aborted = true;
+      } else {
+        tc::fence_after_sync();
+        // l over the 128 token lanes
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float v = l[h];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) lsum_s[warp * 16 + h] = v;
+        }
+        bar_sync(1, 128);
+        float o[G];
+        ld_cols<G>(tO + lane_base, o);  // lane = head_dim index `tid`
+        const bool single = a.n_splits == 1 || L <= a.chunk;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float Lh = lsum_s[h] + lsum_s[16 + h] + lsum_s[32 + h] + lsum_s[48 + h];
+          const float val = o[h] / Lh;
+          const int head = g * G + h;
+          if (single) {
+            static_cast<uint16_t *>(a.out)[((int64_t)b * a.H + head) * kD + tid] = f32_to_bf16_rn(val);
+          } else {
+            const int64_t pidx = ((int64_t)b * a.H + head) * a.max_splits + split;
+            a.o_part[pidx * kD + tid] = val;
+            if (tid == 0) {
+              a.ml_part[pidx * 2] = m[h] * 0.69314718055994531f;
+              a.ml_part[pidx * 2 + 1] = Lh;
+            }
+          }
+        }
+      }
+    }
+    if (aborted) *abort_flag = 1;
+  } else if (warp < 8) {
+    // ================================ loaders =================================================
+    const int lw = warp - 4;
+    const int64_t rowb = (int64_t)a.Hk * kD * 2;  // bytes between consecutive slots
+    const char *kg = static_cast<const char *>(a.k_layer) + (int64_t)g * kD * 2;
+    const char *vg = static_cast<const char *>(a.v_layer) + (int64_t)g * kD * 2;
+    const int half = lane >> 4, c = lane & 15;
+    int64_t nxt = -1;
+    {
+      const int64_t t0 = j0 + lw * 32 + lane;
+      if (ntiles > 0 && t0 < j1) nxt = __ldg(row + t0);
+    }
+    for (int it = 0; it < ntiles; ++it) {
+      const int st = it % kStages;
+      const int64_t tok0 = j0 + (int64_t)it * kTok;
+      int64_t my = nxt;  // slot of token tok0 + lw*32 + lane (or -1 past the chunk)
+      {
+        const int64_t tn = tok0 + kTok + lw * 32 + lane;
+        nxt = (it + 1 < ntiles && tn < j1) ? (int64_t)__ldg(row + tn) : -1;
+      }
+      if (my >= a.size || (my < 0 && tok0 + lw * 32 + lane < j1)) {
+        raise_error(a.err, ASTR_DEVERR_SLOT);
+        my = -1;
+      }
+      int ok = 1;
+      if (lane == 0) {
+        if (it >= kStages) ok = mbar_wait(&empty[st], ((it / kStages) - 1) & 1, a.wait_ns, a.err);
+        if (*abort_flag) ok = 0;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      const uint32_t kst = sbase + kOffK + st * kTileBytes;
+      const uint32_t vst = sbase + kOffV + st * kTileBytes;
+#pragma unroll 4
+      for (int j = 0; j < 16; ++j) {
+        const int tl = j * 2 + half;          // token within this warp's 32
+        const int t = lw * 32 + tl;           // token within the tile
+        const int64_t s = __shfl_sync(0xffffffffu, my, tl);
+        const uint32_t off = tc::sw128_chunk_offset(t, c, kBlockBytes);
+        const bool v = s >= 0;
+        const int64_t go = v ? s * rowb + c * 16 : 0;
+        tc::cp_async16(kst + off, kg + go, v ? 16u : 0u);
+        tc::cp_async16(vst + off, vg + go, v ? 16u : 0u);
+      }
+      tc::cp_async_arrive_noinc(&full[st]);
+    }
+    tc::cp_async_wait_all();
+  } else {
+    // ================================ MMA issuer (one lane) ===================================
+    if (lane == 0) {
+    const uint32_t qaddr = sbase + kOffQ;
+    bool ok = mbar_wait(q_full, 0, a.wait_ns, a.err);
+    auto pv = [&](int i) -> bool {
+      const int sb = i & 1, st = i % kStages;
+      if (!mbar_wait(&p_full[sb], (i >> 1) & 1, a.wait_ns, a.err)) return false;
+      tc::fence_after_sync();
+      tc::fence_proxy_async_smem();
+      const uint32_t vaddr = sbase + kOffV + st * kTileBytes;
+      const uint32_t paddr = sbase + kOffP + sb * 4096;
+#pragma unroll
+      for (int ks = 0; ks < kTok / 16; ++ks) {
+        const uint64_t ad = tc::desc_sw128(vaddr + ks * 2048, kBlockBytes, 1024);
+        const uint64_t bd = tc::desc_sw128(paddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
+        tc::mma_ss(tO, ad, bd, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+      }
+      tc::mma_commit(&empty[st]);
+      tc::mma_commit(&pv_done[sb]);
+      return true;
+    };
+    if (ok) {
+      tc::fence_after_sync();
+      for (int it = 0; it < ntiles && ok; ++it) {
+        const int st = it % kStages, sb = it & 1;
+        if (*abort_flag || !mbar_wait(&full[st], (it / kStages) & 1, a.wait_ns, a.err)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        tc::fence_proxy_async_smem();
+        const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint64_t ad = tc::desc_sw128(kaddr + (ks >> 2) * kBlockBytes + (ks & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::desc_sw128(qaddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
+          tc::mma_ss(tS0 + sb * 16, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&s_full[sb]);
+        if (it > 0 && !pv(it - 1)) ok = false;
+      }
+      if (ok && ntiles > 0 && !pv(ntiles - 1)) ok = false;
+    }
+    if (!ok) *abort_flag = 1;
+    tc::mma_commit(drain);  // nothing may still be in flight when TMEM is freed
+    mbar_wait(drain, 0, kDrainLimitNs, a.err);
+    }
+    __syncwarp();
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 64);
+  }
+}
+
+template <int G>
+cudaError_t run_g(const DecArgs &a, int64_t grid, cudaStream_t s) {
+  auto k = decode_tc_kernel<G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_decode_supported(int dtype, int head_dim, int group) {
+  return dtype == ASTR_BF16 && head_dim == kD &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+int tc_decode_tile_tokens() { return kTok; }
+
+cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const void *q,
+                             int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream) {
+  DecArgs a;
+  const int64_t layer_elems = (int64_t)layer_id * kv.size * kv.n_kv_heads * kv.head_dim;
+  a.q = q;
+  a.k_layer = static_cast<const char *>(kv.k_buffer) + layer_elems * 2;
+  a.v_layer = static_cast<const char *>(kv.v_buffer) + layer_elems * 2;
+  a.r2t = kv.req_to_token;
+  a.rpi = kv.req_pool_indices;
+  a.seq_lens = kv.seq_lens;
+  a.o_part = kv.decode_o_part;
+  a.ml_part = kv.decode_ml_part;
+  a.out = kv.decode_out;
+  a.size = kv.size;
+  a.wait_ns = plan.wait_ns;
+  a.err = plan.err;
+  a.num_reqs = kv.num_reqs;
+  a.max_ctx = kv.max_ctx_len;
+  a.H = n_heads;
+  a.Hk = kv.n_kv_heads;
+  a.B = kv.batch;
+  a.chunk = plan.chunk;
+  a.n_splits = plan.n_splits;
+  a.max_splits = kv.max_splits;
+  a.max_len = kv.max_len;
+  a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kv.head_dim));
+  const int64_t grid = (int64_t)kv.batch * plan.n_splits * kv.n_kv_heads;
+  const int G = n_heads / kv.n_kv_heads;
+  cudaError_t e;
+  switch (G) {
+    case 1: e = run_g<1>(a, grid, stream); break;
+    case 2: e = run_g<2>(a, grid, stream); break;
+    case 4: e = run_g<4>(a, grid, stream); break;
+    case 8: e = run_g<8>(a, grid, stream); break;
+    case 16: e = run_g<16>(a, grid, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  if (plan.n_splits > 1) return launch_split_merge(kv, n_heads, plan, stream);
+  return cudaSuccess;
+}
+
+}  // namespace astr

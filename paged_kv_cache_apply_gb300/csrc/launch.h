@@ -1,0 +1,53 @@
+// Internal launchers behind the C ABI (host side). Each returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/astr.h"
+
+namespace astr {
+
+cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, const void *q,
+                                 void *q_out, const void *k, const void *v, int32_t n_heads,
+                                 const float *freqs, int32_t freqs_max_len,
+                                 const int32_t *position_ids, cudaStream_t stream, int num_sms,
+                                 uint32_t *err);
+
+// Chunked attention on the CUDA cores: decode (mode 0, one query per request, split into
+// `chunk`-token pieces) or f32 prefill rows (mode 1, one query per packed row, unsplit).
+struct SimtAttnPlan {
+  int mode;        // 0 decode, 1 prefill rows
+  int chunk;       // decode: tokens per split
+  int n_splits;    // decode: ceil(max_len / chunk)
+  uint64_t wait_ns;
+  uint32_t *err;   // device error word
+};
+
+bool simt_attn_supported(int dtype, int head_dim, int group);
+cudaError_t launch_simt_attention(const astr_kv_cache &kv, int32_t layer_id, const void *q,
+                                  void *out, int32_t n_heads, const SimtAttnPlan &plan,
+                                  cudaStream_t stream);
+int simt_tile_tokens(int group);
+
+// log-sum-exp merge of the decode split-K partials into decode_out
+cudaError_t launch_split_merge(const astr_kv_cache &kv, int32_t n_heads, const SimtAttnPlan &plan,
+                               cudaStream_t stream);
+
+// tcgen05 bf16 decode (head_dim 128)
+bool tc_decode_supported(int dtype, int head_dim, int group);
+int tc_decode_tile_tokens();
+cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const void *q,
+                             int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream);
+
+// tcgen05 bf16 prefill.
+bool tc_prefill_supported(int dtype, int head_dim, int group, int q_tile_rows);
+cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const void *q,
+                              void *out, int32_t n_heads, uint64_t wait_ns, uint32_t *err,
+                              cudaStream_t stream);
+
+// checked mode: device-side validation of the index metadata
+cudaError_t launch_validate(const astr_kv_cache &kv, int what, uint32_t *err, cudaStream_t stream);
+enum { VALIDATE_DECODE = 1, VALIDATE_PREFILL = 2 };
+
+}  // namespace astr

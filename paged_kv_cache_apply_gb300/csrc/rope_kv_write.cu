@@ -1,0 +1,178 @@
+// Fused RoPE + KV cache write.
+//
+// AstrAI internals, "Rotary Position Embedding (RoPE)": freqs_cis [max_len, dim/2, 2] f32
+// [cos, sin] pairs indexed by position_ids; RoPE is applied before the KV cache write.
+// AstrAI inference guide, "KVCache System": k_buffer[layer_id, out_cache_loc] = k;
+// "Rotary Embedding Backend": the complex product pairs adjacent elements (x[2i], x[2i+1]).
+//
+// One thread handles one 8-element chunk (4 rotation pairs) of one head row of one token:
+// a 16-byte (bf16) or 32-byte (f32) load of the row chunk plus a 32-byte load of the four
+// (cos, sin) pairs, the rotation in f32 with separately rounded products and sums, and one
+// coalesced store -- to q_out for query heads, to the cache row out_cache_loc[t] for key
+// heads (rotated) and value heads (copied). Every 1 KB cache row is written by contiguous
+// threads, so the scatter stays fully coalesced.
+#include "astr_internal.cuh"
+#include "launch.h"
+
+namespace astr {
+
+namespace {
+
+struct RopeArgs {
+  const void *q;
+  void *q_out;
+  const void *k;
+  const void *v;
+  void *k_layer;  // k_buffer + layer_id * size * Hk * D
+  void *v_layer;
+  const float *freqs;
+  const int32_t *pos;
+  const int32_t *loc;
+  int64_t n_tokens;
+  int64_t size;
+  int32_t freqs_max_len;
+  int32_t H, Hk, D;
+  uint32_t *err;
+};
+
+__device__ __forceinline__ void rotate4(const float (&x)[8], const float (&cs)[8], float (&y)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = x[2 * i], b = x[2 * i + 1], c = cs[2 * i], s = cs[2 * i + 1];
+    y[2 * i] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+    y[2 * i + 1] = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
+  }
+}
+
+template <typename T>
+struct Chunk;
+
+template <>
+struct Chunk<float> {
+  static __device__ __forceinline__ void load(const void *base, int64_t off, float (&x)[8]) {
+    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + off);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  static __device__ __forceinline__ void store(void *base, int64_t off, const float (&y)[8]) {
+    float4 *p = reinterpret_cast<float4 *>(static_cast<float *>(base) + off);
+    p[0] = make_float4(y[0], y[1], y[2], y[3]);
+    p[1] = make_float4(y[4], y[5], y[6], y[7]);
+  }
+  static __device__ __forceinline__ void copy(const void *src, int64_t so, void *dst, int64_t dof) {
+    const float4 *s = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + so);
+    float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(dst) + dof);
+    d[0] = __ldg(s);
+    d[1] = __ldg(s + 1);
+  }
+};
+
+template <>
+struct Chunk<bf16_t> {
+  static __device__ __forceinline__ void load(const void *base, int64_t off, float (&x)[8]) {
+    uint4 w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + off));
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+  }
+  static __device__ __forceinline__ void store(void *base, int64_t off, const float (&y)[8]) {
+    uint4 w;
+    w.x = pack_bf16x2_rn(y[0], y[1]);
+    w.y = pack_bf16x2_rn(y[2], y[3]);
+    w.z = pack_bf16x2_rn(y[4], y[5]);
+    w.w = pack_bf16x2_rn(y[6], y[7]);
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + off) = w;
+  }
+  static __device__ __forceinline__ void copy(const void *src, int64_t so, void *dst, int64_t dof) {
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst) + dof) =
+        __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(src) + so));
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
+  const int chunks_per_row = a.D >> 3;
+  const int rows = a.H + 2 * a.Hk;
+  const int64_t per_token = (int64_t)rows * chunks_per_row;
+  const int64_t total = a.n_tokens * per_token;
+  for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total;
+       id += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = id / per_token;
+    const int c = (int)(id - t * per_token);
+    const int row = c / chunks_per_row;
+    const int e0 = (c - row * chunks_per_row) << 3;
+    const int32_t p = __ldg(a.pos + t);
+    const int32_t s = __ldg(a.loc + t);
+    const bool pos_ok = p >= 0 && p < a.freqs_max_len;
+    const bool slot_ok = s >= 0 && (int64_t)s < a.size;
+    if (!(pos_ok && slot_ok)) {
+      if (c == 0) raise_error(a.err, (pos_ok ? 0u : ASTR_DEVERR_POS) | (slot_ok ? 0u : ASTR_DEVERR_SLOT));
+      continue;
+    }
+    if (row >= a.H + a.Hk) {  // value head: copied unchanged
+      const int g = row - a.H - a.Hk;
+      Chunk<T>::copy(a.v, (t * a.Hk + g) * a.D + e0, a.v_layer, ((int64_t)s * a.Hk + g) * a.D + e0);
+      continue;
+    }
+    float cs[8];
+    {
+      const float4 *f =
+          reinterpret_cast<const float4 *>(a.freqs + (int64_t)p * a.D + 2 * (e0 >> 1));
+      float4 f0 = __ldg(f), f1 = __ldg(f + 1);
+      cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+      cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
+    }
+    float x[8], y[8];
+    if (row < a.H) {
+      const int64_t off = (t * a.H + row) * a.D + e0;
+      Chunk<T>::load(a.q, off, x);
+      rotate4(x, cs, y);
+      Chunk<T>::store(a.q_out, off, y);
+    } else {
+      const int g = row - a.H;
+      Chunk<T>::load(a.k, (t * a.Hk + g) * a.D + e0, x);
+      rotate4(x, cs, y);
+      Chunk<T>::store(a.k_layer, ((int64_t)s * a.Hk + g) * a.D + e0, y);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, const void *q,
+                                 void *q_out, const void *k, const void *v, int32_t n_heads,
+                                 const float *freqs, int32_t freqs_max_len,
+                                 const int32_t *position_ids, cudaStream_t stream,
+                                 int num_sms, uint32_t *err) {
+  RopeArgs a;
+  const size_t esz = kv.dtype == ASTR_BF16 ? 2 : 4;
+  const int64_t layer_elems = (int64_t)layer_id * kv.size * kv.n_kv_heads * kv.head_dim;
+  a.q = q;
+  a.q_out = q_out;
+  a.k = k;
+  a.v = v;
+  a.k_layer = static_cast<char *>(kv.k_buffer) + layer_elems * esz;
+  a.v_layer = static_cast<char *>(kv.v_buffer) + layer_elems * esz;
+  a.freqs = freqs;
+  a.pos = position_ids;
+  a.loc = kv.out_cache_loc;
+  a.n_tokens = kv.n_tokens;
+  a.size = kv.size;
+  a.freqs_max_len = freqs_max_len;
+  a.H = n_heads;
+  a.Hk = kv.n_kv_heads;
+  a.D = kv.head_dim;
+  a.err = err;
+  const int64_t total = kv.n_tokens * (int64_t)(n_heads + 2 * kv.n_kv_heads) * (kv.head_dim / 8);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms * 32;
+  if (blocks > cap) blocks = cap;
+  if (kv.dtype == ASTR_BF16)
+    rope_kv_write_kernel<bf16_t><<<(unsigned)blocks, 256, 0, stream>>>(a);
+  else
+    rope_kv_write_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace astr

@@ -1,0 +1,155 @@
+"""Device plumbing: upload a seeded workload with torch, build the KVCache views, run steps.
+
+Data movement and argument marshalling only; every step runs in libastr's kernels through
+the binding in this package.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+from . import (KVCache, astr_decode_attention, astr_prefill_attention, astr_rope_kv_write)
+from .workloads import Workload
+
+
+def to_torch(arr: np.ndarray, dtype: str, device="cuda", pin: bool = False):
+    """Host array -> torch tensor. bf16 data arrives as uint16 bit patterns."""
+    import torch
+    a = np.ascontiguousarray(arr)
+    if dtype == "bf16":
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    elif dtype == "f32":
+        t = torch.from_numpy(a.astype(np.float32, copy=False))
+    elif dtype == "i32":
+        t = torch.from_numpy(a.astype(np.int32, copy=False))
+    else:
+        raise ValueError(dtype)
+    if device == "cpu":
+        return t.pin_memory() if pin else t
+    return t.to(device)
+
+
+def to_host(t) -> np.ndarray:
+    """torch tensor -> numpy (bf16 -> uint16 bits)."""
+    import torch
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+@dataclass
+class DeviceWorkload:
+    wl: Workload
+    k_buffer: object
+    v_buffer: object
+    req_to_token: object
+    n_heads: int
+    rope: Optional[dict] = None
+    rope2: Optional[dict] = None
+    prefill: Optional[dict] = None
+    decode: Optional[dict] = None
+    decode2: Optional[dict] = None
+
+    # ------------------------------------------------------------------
+    @classmethod
+    def upload(cls, wl: Workload, device="cuda") -> "DeviceWorkload":
+        import torch
+        dt = wl.pool.dtype
+        dw = cls(wl=wl, k_buffer=to_torch(wl.pool.k_buffer, dt, device),
+                 v_buffer=to_torch(wl.pool.v_buffer, dt, device),
+                 req_to_token=to_torch(wl.pool.req_to_token, "i32", device), n_heads=wl.n_heads)
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+
+        def rope_dict(r):
+            if r is None:
+                return None
+            d = dict(q=to_torch(r.q, dt, device), k=to_torch(r.k, dt, device),
+                     v=to_torch(r.v, dt, device), pos=to_torch(r.position_ids, "i32", device),
+                     loc=to_torch(r.out_cache_loc, "i32", device),
+                     freqs=to_torch(r.freqs_cis, "f32", device), layer=r.layer_id)
+            d["q_out"] = torch.empty_like(d["q"])
+            d["kv"] = KVCache(dw.k_buffer, dw.v_buffer, out_cache_loc=d["loc"])
+            return d
+
+        dw.rope = rope_dict(wl.rope)
+        dw.rope2 = rope_dict(wl.rope2)
+
+        def q_of(batch, rope, rows):
+            if batch.q is not None:
+                return to_torch(batch.q, dt, device)
+            return rope["q_out"][batch.q_token_offset: batch.q_token_offset + rows]
+
+        if wl.prefill is not None:
+            p = wl.prefill
+            q = q_of(p, dw.rope, p.total_q)
+            d = dict(q=q, out=torch.empty((p.total_q, wl.n_heads, wl.pool.head_dim), dtype=tdt,
+                                          device=device), layer=p.layer_id)
+            d["kv"] = KVCache(dw.k_buffer, dw.v_buffer, req_to_token=dw.req_to_token,
+                              req_pool_indices=to_torch(p.req_pool_indices, "i32", device),
+                              qo_indptr=to_torch(p.qo_indptr, "i32", device),
+                              kv_indptr=to_torch(p.kv_indptr, "i32", device),
+                              q_tile_to_batch=to_torch(p.q_tile_to_batch, "i32", device),
+                              q_tile_to_index=to_torch(p.q_tile_to_index, "i32", device),
+                              q_tile_rows=p.q_tile_rows, n_tokens=p.total_q)
+            dw.prefill = d
+
+        def decode_dict(dec, rope):
+            if dec is None:
+                return None
+            q = q_of(dec, rope, dec.batch)
+            H, D = wl.n_heads, wl.pool.head_dim
+            d = dict(q=q, layer=dec.layer_id,
+                     out=torch.empty((dec.batch, H, D), dtype=tdt, device=device),
+                     o_part=torch.empty((dec.batch, H, dec.max_splits, D), dtype=torch.float32,
+                                        device=device),
+                     ml_part=torch.empty((dec.batch, H, dec.max_splits, 2), dtype=torch.float32,
+                                         device=device))
+            d["kv"] = KVCache(dw.k_buffer, dw.v_buffer, req_to_token=dw.req_to_token,
+                              req_pool_indices=to_torch(dec.req_pool_indices, "i32", device),
+                              seq_lens=to_torch(dec.seq_lens, "i32", device), max_len=dec.max_len,
+                              kv_indptr=to_torch(dec.kv_indptr, "i32", device),
+                              decode_o_part=d["o_part"], decode_ml_part=d["ml_part"],
+                              split_chunk=dec.split_chunk, decode_out=d["out"])
+            return d
+
+        dw.decode = decode_dict(wl.decode, dw.rope)
+        dw.decode2 = decode_dict(wl.decode2, dw.rope2)
+        return dw
+
+    # ------------------------------------------------------------------
+    @staticmethod
+    def _c(d):
+        """The C struct of a step's KVCache, built once (call refresh() after editing fields)."""
+        if "c" not in d:
+            d["c"] = d["kv"].as_c()
+        return d["c"]
+
+    def refresh(self):
+        for d in [self.rope, self.rope2, self.prefill, self.decode, self.decode2]:
+            if d is not None:
+                d.pop("c", None)
+
+    def run_rope(self, which="rope", stream=None):
+        r = getattr(self, which)
+        astr_rope_kv_write(self._c(r), r["layer"], r["q"], r["q_out"], r["k"], r["v"],
+                           self.n_heads, r["freqs"], r["freqs"].shape[0], r["pos"], stream)
+
+    def run_prefill(self, stream=None):
+        p = self.prefill
+        astr_prefill_attention(self._c(p), p["layer"], p["q"], p["out"], self.n_heads, stream)
+
+    def run_decode(self, which="decode", stream=None):
+        d = getattr(self, which)
+        astr_decode_attention(self._c(d), d["layer"], d["q"], self.n_heads, stream)
+
+    def run_step(self, stream=None):
+        """One pass of the path over the batch: rotate + write, then prefill, then decode."""
+        if self.rope is not None:
+            self.run_rope("rope", stream)
+        if self.prefill is not None:
+            self.run_prefill(stream)
+        if self.decode is not None:
+            self.run_decode("decode", stream)

@@ -426,3 +426,62 @@ CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
 
 def make(config: int, **kw) -> Workload:
     return CONFIGS[config](**kw)
+
+
+def make_case(dtype: str, n_heads: int, n_kv_heads: int, head_dim: int, page: int, kv_lens,
+              q_lens=None, n_layers: int = 2, layer_id: int = 1, seed: int = SEED_BASE + 100,
+              split_chunk: int = 0, max_splits: int = 16, with_rope: bool = False,
+              freqs_max_len: int = 0) -> Workload:
+    """A small paged case for parametrised tests.
+
+    ``q_lens is None`` builds a decode batch (one query per request at position L-1);
+    otherwise a prefill batch with prefix P_b = kv_lens[b] - q_lens[b]. With ``with_rope`` the
+    newest token of every request (decode) or the request's q_lens new tokens (prefill) are
+    left empty in the cache and produced by a fused rotate + write step, whose q_out feeds the
+    attention call. Every layer of the pool is filled, so a wrong layer offset is visible.
+    """
+    rng = np.random.default_rng([seed, 0])
+    kv_lens = np.asarray(kv_lens, dtype=np.int32)
+    B = kv_lens.size
+    pages = [max(1, (int(n) + page - 1) // page) for n in kv_lens]
+    n_pages = int(np.ceil(1.5 * sum(pages))) + 1
+    max_ctx = int(max(pages) * page)
+    num_reqs = 2 * B + 1
+    pool = _empty_pool(dtype, n_layers, n_pages * page, n_kv_heads, head_dim, page, num_reqs,
+                       max_ctx)
+    rows = rng.permutation(num_reqs)[:B].astype(np.int32)
+    slots = _paged_slots(rng, pages, page, n_pages)
+    decode = q_lens is None
+    qn = np.ones(B, np.int32) if decode else np.asarray(q_lens, dtype=np.int32)
+    cached = []
+    for b in range(B):
+        pool.req_to_token[rows[b], : slots[b].size] = slots[b]
+        upto = int(kv_lens[b] - qn[b]) if with_rope else int(kv_lens[b])
+        cached.append(slots[b][:upto])
+    for lyr in range(n_layers):
+        _fill_rows(pool, np.concatenate(cached), seed, 10 + 2 * lyr, layer=lyr)
+    H, D = n_heads, head_dim
+    rope = None
+    q_total = int(qn.sum())
+    if with_rope:
+        pos = np.concatenate([np.arange(kv_lens[b] - qn[b], kv_lens[b]) for b in range(B)])
+        reqs = np.concatenate([np.full(qn[b], b) for b in range(B)])
+        loc = pool.req_to_token[rows[reqs], pos].astype(np.int32)
+        fm = freqs_max_len or int(kv_lens.max())
+        rope = RopeStep(q=normal_values((q_total, H, D), dtype, seed, 30),
+                        k=normal_values((q_total, n_kv_heads, D), dtype, seed, 31),
+                        v=normal_values((q_total, n_kv_heads, D), dtype, seed, 32),
+                        position_ids=pos.astype(np.int32), out_cache_loc=loc,
+                        freqs_cis=rope_freqs_cis(fm, D), layer_id=layer_id)
+    q = None if with_rope else normal_values((q_total, H, D), dtype, seed, 20)
+    if decode:
+        dec = DecodeBatch(req_pool_indices=rows, seq_lens=kv_lens, kv_indptr=prefix_sum(kv_lens),
+                          max_len=int(kv_lens.max()), q=q, split_chunk=split_chunk,
+                          max_splits=max_splits, layer_id=layer_id)
+        return Workload("case_decode", "parametrised decode case", H, pool, rope=rope, decode=dec,
+                        meta={"seed": seed})
+    tb, ti = q_tiles(qn)
+    pre = PrefillBatch(req_pool_indices=rows, qo_indptr=prefix_sum(qn), kv_indptr=prefix_sum(kv_lens),
+                       q_tile_to_batch=tb, q_tile_to_index=ti, q=q, layer_id=layer_id)
+    return Workload("case_prefill", "parametrised prefill case", H, pool, rope=rope, prefill=pre,
+                    meta={"seed": seed})

@@ -1,0 +1,119 @@
+"""The five configurations at full size, in the launch configuration bench.py times.
+
+Every attention output the oracle can afford is compared (all decode outputs, all prefill rows
+of the mixed batch, a stratified sample of the varlen prefill rows); every written cache row
+and every rotated q row is compared bit for bit, and every other cache row is checked
+unchanged.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_apply_gb300 import build as B
+from paged_kv_cache_apply_gb300 import device as DV
+from paged_kv_cache_apply_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    B.build()
+
+
+def _sync():
+    import torch
+    torch.cuda.synchronize()
+
+
+def wid(a):
+    return W.f32_from_bf16_bits(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def test_config2_decode_page1():
+    wl = W.config2()
+    dw = DV.DeviceWorkload.upload(wl)
+    dw.run_decode()
+    _sync()
+    d = wl.decode
+    ref = oracle.decode(d.q, wl.pool.k_buffer[0], wl.pool.v_buffer[0], wl.pool.req_to_token,
+                        d.req_pool_indices, d.seq_lens)
+    err = np.max(np.abs(wid(DV.to_host(dw.decode["out"])) - ref))
+    assert err <= TOL_BF16, err
+
+
+def test_config3_varlen_resumed_prefill():
+    wl = W.config3()
+    dw = DV.DeviceWorkload.upload(wl)
+    dw.run_prefill()
+    _sync()
+    p = wl.prefill
+    rng = np.random.default_rng(3)
+    rows = set()
+    for b in range(p.batch):
+        q0, q1 = int(p.qo_indptr[b]), int(p.qo_indptr[b + 1])
+        for i in [0, 1, 126, 127, 128, 129, q1 - q0 - 2, q1 - q0 - 1]:
+            if 0 <= i < q1 - q0:
+                rows.add(q0 + i)
+        rows.update(rng.integers(q0, q1, 24).tolist())
+    rows = np.array(sorted(rows), dtype=np.int32)
+    ref = oracle.prefill(p.q, wl.pool.k_buffer[0], wl.pool.v_buffer[0], wl.pool.req_to_token,
+                         p.req_pool_indices, p.qo_indptr, p.kv_indptr, rows=rows)
+    got = wid(DV.to_host(dw.prefill["out"])[rows])
+    err = np.max(np.abs(got - ref))
+    assert err <= TOL_BF16, err
+
+
+def test_config4_long_context_split_decode():
+    wl = W.config4()
+    dw = DV.DeviceWorkload.upload(wl)
+    dw.run_decode()
+    _sync()
+    d = wl.decode
+    kl, vl = wl.pool.k_buffer[0], wl.pool.v_buffer[0]
+    ref = oracle.decode(d.q, kl, vl, wl.pool.req_to_token, d.req_pool_indices, d.seq_lens)
+    err = np.max(np.abs(wid(DV.to_host(dw.decode["out"])) - ref))
+    assert err <= TOL_BF16, err
+    # the fixed 4096-token partials of request 0 against the oracle's
+    one = np.ascontiguousarray(d.q[:1])
+    o_p, m_p, l_p, _ = oracle.decode_split(one, kl, vl, wl.pool.req_to_token,
+                                           d.req_pool_indices[:1], d.seq_lens[:1], 4096,
+                                           d.max_splits)
+    n = (int(d.seq_lens[0]) + 4095) // 4096
+    go = DV.to_host(dw.decode["o_part"])[0, :, :n]
+    gml = DV.to_host(dw.decode["ml_part"])[0, :, :n].astype(np.float64)
+    assert np.max(np.abs(go - o_p[0, :, :n])) <= 1e-3
+    lse = gml[..., 0] + np.log(gml[..., 1])
+    assert np.max(np.abs(lse - (m_p[0, :, :n] + np.log(l_p[0, :, :n])))) <= 1e-3
+
+
+def test_config5_mixed_step():
+    import torch
+    wl = W.config5()
+    dw = DV.DeviceWorkload.upload(wl)
+    k_before = dw.k_buffer.clone()
+    dw.run_step()
+    _sync()
+    kl = np.ascontiguousarray(wl.pool.k_buffer[0]).copy()
+    vl = np.ascontiguousarray(wl.pool.v_buffer[0]).copy()
+    r = wl.rope
+    q_ref = oracle.rope_kv_write(r.q, r.k, r.v, r.freqs_cis, r.position_ids, r.out_cache_loc, kl, vl)
+    assert np.array_equal(DV.to_host(dw.rope["q_out"]), q_ref)
+    loc = torch.from_numpy(r.out_cache_loc.astype(np.int64)).cuda()
+    assert np.array_equal(DV.to_host(dw.k_buffer[0, loc]), kl[r.out_cache_loc])
+    assert np.array_equal(DV.to_host(dw.v_buffer[0, loc]), vl[r.out_cache_loc])
+    changed = (dw.k_buffer != k_before).flatten(2).any(dim=2)[0].nonzero().flatten().cpu().numpy()
+    assert set(changed.tolist()) <= set(r.out_cache_loc.tolist())
+    del k_before
+    p = wl.prefill
+    q_pre = q_ref[p.q_token_offset: p.q_token_offset + p.total_q]
+    ref_p = oracle.prefill(q_pre, kl, vl, wl.pool.req_to_token, p.req_pool_indices, p.qo_indptr,
+                           p.kv_indptr)
+    err_p = np.max(np.abs(wid(DV.to_host(dw.prefill["out"])) - ref_p))
+    assert err_p <= TOL_BF16, err_p
+    d = wl.decode
+    q_dec = np.ascontiguousarray(q_ref[: d.batch])
+    ref_d = oracle.decode(q_dec, kl, vl, wl.pool.req_to_token, d.req_pool_indices, d.seq_lens)
+    err_d = np.max(np.abs(wid(DV.to_host(dw.decode["out"])) - ref_d))
+    assert err_d <= TOL_BF16, err_d
