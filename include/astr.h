@@ -148,6 +148,25 @@ astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, con
                                   int32_t n_heads, astr_stream stream);
 
 /*
+ * Decode that allocates nothing. The pages have no counterpart: it exists for callers that
+ * cannot call cudaMalloc to provide split-K scratch -- plugin hosts that hand a library only
+ * the tensors of one call, embedded runtimes that reserve all device memory at start-up and
+ * forbid later allocations, serving loops that must never block on the allocator.
+ * Computes exactly what astr_decode_attention computes and writes kv->decode_out, but keeps
+ * the split-K partials in an 8 MiB array compiled into this library (one per GPU that loads
+ * it, held until the process exits); kv->decode_o_part, decode_ml_part and max_splits are
+ * ignored. The number of splits is limited to what fits, 8 MiB / (batch * n_heads *
+ * (head_dim + 2) * 4 bytes): with split_chunk = 0 the library picks a chunk that fits, an
+ * explicit split_chunk needing more splits is rejected with ASTR_ERR_INVALID. The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture. Every call shares the array and it keeps the last call's
+ * contents; no entry has to start at zero because each call writes every entry it reads.
+ * Calls whose work overlaps on the GPU (several streams) race on the array.
+ */
+astr_status astr_decode_attention_noalloc(const astr_kv_cache *kv, int32_t layer_id,
+                                          const void *q, int32_t n_heads, astr_stream stream);
+
+/*
  * The split plan astr_decode_attention would use for `kv`: chunk length and the number of
  * splits ceil(max_len / chunk). Host-only; enqueues nothing.
  */

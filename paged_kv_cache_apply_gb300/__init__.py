@@ -65,6 +65,7 @@ def lib():
             KV = C.POINTER(astr_kv_cache)
             L.astr_rope_kv_write.argtypes = [KV, I32, P, P, P, P, I32, P, I32, P, P]
             L.astr_decode_attention.argtypes = [KV, I32, P, I32, P]
+            L.astr_decode_attention_noalloc.argtypes = [KV, I32, P, I32, P]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
             L.astr_prefill_attention.argtypes = [KV, I32, P, P, I32, P]
             L.astr_last_error.restype = C.c_char_p
@@ -75,6 +76,7 @@ def lib():
             L.astr_version.restype = I32
             L.astr_kv_cache_bytes.restype = I32
             for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
+                         "astr_decode_attention_noalloc",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -204,6 +206,13 @@ def astr_decode_attention(kv, layer_id, q, n_heads, stream=None) -> None:
     c = _kv(kv)
     _check(lib().astr_decode_attention(C.byref(c), int(layer_id), _ptr(q), int(n_heads),
                                        _stream(stream)))
+
+
+def astr_decode_attention_noalloc(kv, layer_id, q, n_heads, stream=None) -> None:
+    """Decode without caller scratch: for callers that cannot allocate device memory."""
+    c = _kv(kv)
+    _check(lib().astr_decode_attention_noalloc(C.byref(c), int(layer_id), _ptr(q), int(n_heads),
+                                               _stream(stream)))
 
 
 def astr_decode_plan(kv, n_heads):

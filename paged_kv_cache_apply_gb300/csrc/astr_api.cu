@@ -200,6 +200,8 @@ __global__ void selftest_wait_kernel(uint64_t ns, uint32_t *err) {
 }
 }  // namespace
 
+void set_last_error_message(const char *msg) { t_last_error = msg ? msg : ""; }
+
 cudaError_t launch_validate(const astr_kv_cache &kv, int what, uint32_t *err, cudaStream_t stream) {
   validate_kernel<<<1, 1024, 0, stream>>>(kv, what, err);
   return cudaGetLastError();

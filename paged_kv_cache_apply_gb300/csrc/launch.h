@@ -46,6 +46,9 @@ cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const v
                               void *out, int32_t n_heads, uint64_t wait_ns, uint32_t *err,
                               cudaStream_t stream);
 
+// sets the message astr_last_error() returns on this thread
+void set_last_error_message(const char *msg);
+
 // checked mode: device-side validation of the index metadata
 cudaError_t launch_validate(const astr_kv_cache &kv, int what, uint32_t *err, cudaStream_t stream);
 enum { VALIDATE_DECODE = 1, VALIDATE_PREFILL = 2 };
