@@ -85,7 +85,7 @@ typedef struct astr_kv_cache {
   int32_t batch;
   int32_t max_len;                 /* host int: max(seq_lens) (decode grid sizing, no sync) */
   const int32_t *out_cache_loc;    /* [n_tokens] write slots of this forward */
-  int64_t n_tokens;
+  int64_t n_tokens;                /* new tokens of this forward (prefill: packed q rows) */
   const int32_t *kv_indptr;        /* [batch+1] prefix sum of kv lengths */
   const int32_t *qo_indptr;        /* [batch+1] prefix sum of q lengths (prefill) */
   const int32_t *q_tile_to_batch;  /* [num_q_tiles] prefill: tile -> request */
@@ -185,7 +185,9 @@ astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *
  * Row i of request b sits at absolute position P_b + i, P_b = K_b - Q_b (the cached prefix),
  * and attends keys j <= P_b + i:
  *   out[t, h, :] = sum_{j <= P_b+i} softmax_j(q[t,h,:] . K_j / sqrt(d)) V_j.
- * The new tokens' K/V (positions P_b..K_b-1) must already be in the cache. Tile t covers
+ * The new tokens' K/V (positions P_b..K_b-1) must already be in the cache; kv->n_tokens is
+ * the number of packed q rows, qo_indptr[batch] (n_layers * size must stay below 2^31 for the
+ * bf16 path, whose row coordinates are 32-bit). Tile t covers
  * request q_tile_to_batch[t], rows [q_tile_rows * q_tile_to_index[t], +q_tile_rows) clipped
  * to Q_b; together the tiles must cover every row exactly once. Rows are written only by
  * their tile. bf16 runs on the tcgen05 tensor cores (bf16 operands, f32 accumulation);

@@ -358,6 +358,9 @@ astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, co
     return cuda_fail(e, "checked-mode validation launch");
   const uint64_t wait_ns = (uint64_t)g_wait_ns.load();
   if (kv->dtype == ASTR_BF16 && tc_prefill_supported(kv->dtype, kv->head_dim, G, kv->q_tile_rows)) {
+    if (!tc_prefill_fits(*kv))
+      return fail(ASTR_ERR_INVALID, "bf16 prefill needs n_tokens = the number of packed q rows (got %lld) "
+                  "and n_layers * size < 2^31", (long long)kv->n_tokens);
     e = launch_tc_prefill(*kv, layer_id, q, out, n_heads, wait_ns, err, s);
   } else {
     if (!simt_attn_supported(kv->dtype, kv->head_dim, G))

@@ -42,6 +42,7 @@ cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const vo
 
 // tcgen05 bf16 prefill.
 bool tc_prefill_supported(int dtype, int head_dim, int group, int q_tile_rows);
+bool tc_prefill_fits(const astr_kv_cache &kv);  // n_tokens set, row coordinates within int32
 cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const void *q,
                               void *out, int32_t n_heads, uint64_t wait_ns, uint32_t *err,
                               cudaStream_t stream);

@@ -8,18 +8,23 @@
 // with prefix P sits at P + i).
 //
 // One block computes a 128-row Q tile for NQ = 2 query heads of the same KV group (1 when
-// the group has a single head), so every K/V tile it stages feeds two heads:
-//  * warps 8-11 stream the two Q tiles once and then 128-key K and V tiles (two stages each,
-//    released separately) with 16-byte cp.async copies into the 128-byte-swizzled layout,
-//    zero-filling keys past the request;
-//  * warp 12 allocates all 512 TMEM columns -- S0 | S1 | O0 | O1, 128 each -- and issues the
-//    MMAs head by head, S_h = Q_h K^T (M = N = K = 128) and O_h += P_h V (P_h read from TMEM
-//    where the softmax wrote it over S_h, V an MN-major operand), interleaving the heads so
-//    the tensor core works on one head while the other head's softmax runs;
-//  * warps 0-3 and 4-7 are the softmax of head 0 and head 1, one row per thread: a pass for
-//    the row max, the reference max raised only when the row max exceeds it by 2^8 (the O row
-//    is then rescaled in TMEM; the commit that published S also covers the previous P.V),
-//    a pass writing exp2 of the scaled scores as bf16 P, and the epilogue that normalises O.
+// the group has a single head), so every K/V tile it stages feeds two heads; when the group
+// has two or more such pairs, the blocks of two pairs form a cluster and each K/V box is
+// fetched once and multicast into both blocks' shared memory:
+//  * warp 16 streams the two Q tiles once and then 128-key K and V tiles (two stages each,
+//    released separately) into the 128-byte-swizzled layout: one TMA tensor copy of a 16-row
+//    box per run of 16 keys whose slots are consecutive (a page; destinations 2 KB aligned),
+//    16-byte cp.async copies for keys outside such runs, zero-filled past the request;
+//  * warp 17 allocates all 512 TMEM columns -- S0 | S1 | O0 | O1, 128 each -- and warps 17
+//    and 18 each issue one head's MMAs, S_h = Q_h K^T (M = N = K = 128) and O_h += P_h V
+//    (P_h read from TMEM where the softmax wrote it over S_h, V an MN-major operand); with one
+//    issuer per head the tensor core works on one head while the other head's softmax runs;
+//  * warps 0-7 and 8-15 are the softmax of head 0 and head 1, two threads per row (64 scores
+//    each, partial maxima exchanged through shared memory): a pass for the row max, the
+//    reference max raised only when the row max exceeds it by 2^8 (the O row is then rescaled
+//    in TMEM; the commit that published S also covers the previous P.V), a pass writing exp2
+//    of the scaled scores as bf16 P over the thread's own half of S, and the epilogue that
+//    normalises O.
 // KV tiles beyond the diagonal of the tile are skipped; the mask is applied only to tiles
 // that cross the diagonal or the end of the request. All waits are bounded.
 #include <math.h>
@@ -27,6 +32,7 @@
 #include "astr_internal.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
+#include "tma_maps.h"
 
 namespace astr {
 
@@ -37,13 +43,14 @@ constexpr int kKeys = 128;                 // keys per KV tile (N of S, K of P.V
 constexpr int kD = 128;
 constexpr int kTile = kRows * kD * 2;      // 32 KB: one Q, K or V tile
 constexpr int kBlk = kRows * 128;          // 16 KB: one 64-element half
-constexpr int kThreads = 416;              // 8 softmax + 4 loader + 1 MMA warps
+constexpr int kThreads = 608;              // 16 softmax + 1 loader + 2 MMA warps
 constexpr float kLazyRescale = 8.0f;
 
 constexpr int kOffQ = 0;                   // 2 Q tiles
 constexpr int kOffK = kOffQ + 2 * kTile;   // 2 K stages
 constexpr int kOffV = kOffK + 2 * kTile;   // 2 V stages
-constexpr int kOffBar = kOffV + 2 * kTile;
+constexpr int kOffRed = kOffV + 2 * kTile;   // [2 heads][3 bufs][2 halves][128] f32
+constexpr int kOffBar = kOffRed + 2 * 3 * 2 * 128 * 4;
 constexpr int kOffMisc = kOffBar + 32 * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
 
@@ -63,6 +70,8 @@ struct PreArgs {
   const int32_t *tile_i;
   int64_t size;
   int64_t n_rows;  // packed q rows
+  int32_t layer_row0;  // first row of this layer in the [n_layers * size, Hk * D] view
+  int32_t total_rows;  // n_layers * size: any row at or past it reads as zero
   uint64_t wait_ns;
   uint32_t *err;
   int32_t num_reqs, max_ctx;
@@ -82,16 +91,18 @@ __device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
   return r != 0;
 }
 
-template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a) {
+template <int NQ, bool MC>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PreArgs a, const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap k16, const __grid_constant__ CUtensorMap v16) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-  uint64_t *q_full = bars;           // loaders -> MMA (128 arrivals)
-  uint64_t *k_full = bars + 1;       // [2]
-  uint64_t *v_full = bars + 3;       // [2]
+  uint64_t *q_full = bars;           // TMA -> MMA (transaction bytes)
+  uint64_t *k_full = bars + 1;       // [2] TMA -> MMA
+  uint64_t *v_full = bars + 3;       // [2] TMA -> MMA
   uint64_t *k_empty = bars + 5;      // [2] MMA commit
   uint64_t *v_empty = bars + 7;      // [2] MMA commit
   uint64_t *s_full = bars + 9;       // [2] per head, MMA commit
@@ -142,37 +153,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a
 
   // ---- set-up ---------------------------------------------------------------------------------
   if (tid == 0) {
-    mbar_init(q_full, 128);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 128);
-      mbar_init(&v_full[i], 128);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_empty[i], 1);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {  // 32 loader lanes (cp.async) + one expect-tx arrival (TMA)
+      mbar_init(&k_full[i], 33);
+      mbar_init(&v_full[i], 33);
+      mbar_init(&k_empty[i], NQ * (MC ? 2 : 1));  // one commit per head issuer, per CTA
+      mbar_init(&v_empty[i], NQ * (MC ? 2 : 1));
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 256);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, NQ);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 12) {
+  if (warp == 17) {
     tc::tmem_alloc(tmem_slot, 512);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+  if constexpr (MC)
+    tc::cluster_sync();  // both CTAs' barriers exist before either copies or commits into them
+  else
+    __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t crank = MC ? tc::cluster_ctarank() : 0;
 
-  if (warp < 8) {
-    // ======================= softmax of head h = warp / 4, row = tid % 128 =======================
-    const int h = warp >> 2;
-    const int r = tid & 127;
+  if (warp < 16) {
+    // ============ softmax: head h = warp / 8, column half cb = (warp / 4) & 1, row = lane quarter
+    // Two threads own a row: each reads 64 of its 128 scores, they exchange their partial maxima
+    // through shared memory once per tile, and each writes its 64 P values into the first 32
+    // columns of its own half of S, so neither overwrites scores the other still has to read.
+    const int h = warp >> 3;
+    const int cb = (warp >> 2) & 1;
+    const int r = (warp & 3) * 32 + lane;
     if (h < NQ) {
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-      const uint32_t tS = tmem + h * 128 + lane_base;
-      const uint32_t tO = tmem + 256 + h * 128 + lane_base;
+      const uint32_t tS = tmem + h * 128 + cb * 64 + lane_base;
+      const uint32_t tO = tmem + 256 + h * 128 + cb * 64 + lane_base;
+      // [3 buffers][2 halves][128 rows]: tile maxima alternate between 0 and 1, 2 is for the sums
+      float *xred = reinterpret_cast<float *>(smem + kOffRed) + h * 3 * 2 * 128;
       const int64_t pos = Pb + r0 + r;  // absolute position of this row
       const int64_t pos_min = Pb + r0;
       float m = -INFINITY, l = 0.f;
@@ -180,37 +201,49 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a
       const int bar_id = 1 + h;
       for (int j = 0; j < nkv; ++j) {
         const bool ok = mbar_wait(&s_full[h], j & 1, a.wait_ns, a.err);
-        if (bar_any(bar_id, 128, !ok)) {
+        const int64_t k0 = (int64_t)j * kKeys + cb * 64;  // first key of my half
+        const bool masked = ((int64_t)j * kKeys + kKeys - 1 > pos_min) || ((int64_t)j * kKeys + kKeys > Kb);
+        int nvalid = 64;
+        if (masked) {
+          const int64_t lim = (pos + 1 < Kb ? pos + 1 : Kb) - k0;
+          nvalid = lim < 0 ? 0 : (lim > 64 ? 64 : (int)lim);
+        }
+        float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
+        if (ok) {
+          tc::fence_after_sync();
+          uint32_t buf[2][32];
+          tc::tmem_ld32(tS, buf[0]);
+          tc::tmem_ld32(tS + 32, buf[1]);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t *sv = buf[c];
+            if (masked) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (c * 32 + k >= nvalid) sv[k] = 0xFF800000u;  // -inf
+            }
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+              mxa = fmax3(mxa, __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
+              mxb = fmax3(mxb, __uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3]));
+              mxc = fmax3(mxc, __uint_as_float(sv[k + 4]), __uint_as_float(sv[k + 5]));
+              mxd = fmax3(mxd, __uint_as_float(sv[k + 6]), __uint_as_float(sv[k + 7]));
+            }
+          }
+          xred[((j & 1) * 2 + cb) * 128 + r] = fmax3(mxa, mxb, fmaxf(mxc, mxd));
+        }
+        if (bar_any(bar_id, 256, !ok)) {  // also publishes the partial maxima
           aborted = true;
           break;
         }
-        tc::fence_after_sync();
-        const int64_t k0 = (int64_t)j * kKeys;
-        const bool masked = (k0 + kKeys - 1 > pos_min) || (k0 + kKeys > Kb);
-        // pass 1: row max of the raw scores
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t s[32];
-          tc::tmem_ld32(tS + c * 32, s);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            float v = __uint_as_float(s[k]);
-            if (masked) {
-              const int64_t key = k0 + c * 32 + k;
-              if (key > pos || key >= Kb) v = -INFINITY;
-            }
-            mx = fmaxf(mx, v);
-          }
-        }
-        mx *= a.scale_log2;
+        const float mx = fmaxf(xred[((j & 1) * 2 + 0) * 128 + r], xred[((j & 1) * 2 + 1) * 128 + r]) * a.scale_log2;
         const float m_new = (mx > m + kLazyRescale) ? mx : m;
         const float alpha = ex2_approx(m - m_new);
         if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
           // the commit behind s_full also covers P.V of the previous tile: O is settled
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
             tc::tmem_ld32(tO + c * 32, o);
             tc::tmem_ld_wait();
@@ -223,45 +256,52 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a
         }
         l *= alpha;
         m = m_new;
-        // pass 2: P = exp2(score * scale - m) in bf16, written over S (column pairs)
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t s[32];
-          tc::tmem_ld32(tS + c * 32, s);
+        // P = exp2(score * scale - m) in bf16, into columns [0, 32) of my half of S
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nm2 = make_float2(-m, -m);
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+        {
+          uint32_t buf[2][32];
+          tc::tmem_ld32(tS, buf[0]);
+          tc::tmem_ld32(tS + 32, buf[1]);
           tc::tmem_ld_wait();
-          uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            float x0 = __uint_as_float(s[k]) * a.scale_log2 - m;
-            float x1 = __uint_as_float(s[k + 1]) * a.scale_log2 - m;
-            if (masked) {
-              const int64_t key = k0 + c * 32 + k;
-              if (key > pos || key >= Kb) x0 = -INFINITY;
-              if (key + 1 > pos || key + 1 >= Kb) x1 = -INFINITY;
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t *sv = buf[c];
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float2 x = ffma2(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sc2, nm2);
+              float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              if (masked) {
+                if (c * 32 + k >= nvalid) p0 = 0.f;
+                if (c * 32 + k + 1 >= nvalid) p1 = 0.f;
+              }
+              sum2[(k >> 1) & 3] = fadd2(sum2[(k >> 1) & 3], make_float2(p0, p1));
+              pk[k >> 1] = pack_bf16x2_rn(p0, p1);
             }
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            sum += p0 + p1;
-            pk[k >> 1] = pack_bf16x2_rn(p0, p1);
+            tc::tmem_st16(tS + c * 16, pk);
           }
-          tc::tmem_st16(tS + c * 16, pk);
         }
-        l += sum;
+        const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
+        l += (s01.x + s01.y) + (s23.x + s23.y);
         tc::tmem_st_wait();
         tc::fence_before_sync();
         mbar_arrive(&p_full[h]);
       }
       if (!aborted && nkv > 0) {
         const bool ok = mbar_wait(&o_done[h], 0, a.wait_ns, a.err);
-        if (bar_any(bar_id, 128, !ok)) {
+        xred[(2 * 2 + cb) * 128 + r] = l;  // both partial sums of the row
+        if (bar_any(bar_id, 256, !ok)) {
           aborted = true;
         } else {
           tc::fence_after_sync();
-          const float inv = 1.f / l;
-          uint16_t *orow = static_cast<uint16_t *>(a.out) + ((q0 + r0 + r) * a.H + h0 + h) * kD;
+          const float inv = 1.f / (xred[4 * 128 + r] + xred[5 * 128 + r]);
+          uint16_t *orow = static_cast<uint16_t *>(a.out) + ((q0 + r0 + r) * a.H + h0 + h) * kD + cb * 64;
           const bool write = (int64_t)r < rows_here;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
             tc::tmem_ld32(tO + c * 32, o);
             tc::tmem_ld_wait();
@@ -281,97 +321,100 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a
       }
       if (aborted) *abort_flag = 1;
     }
-  } else if (warp < 12) {
-    // ================================ loaders ==================================================
-    const int lt = tid - 256;      // 0..127
-    const int lw = lt >> 5;
-    const int half = lane >> 4, c = lane & 15;
+  } else if (warp == 16) {
+    // ============================== TMA loader (one warp) ======================================
+    const int col0 = g * kD;  // this KV head's columns in the [rows, Hk * D] view
     const int64_t rowb_kv = (int64_t)a.Hk * kD * 2;
-    const char *kg = static_cast<const char *>(a.k_layer) + (int64_t)g * kD * 2;
-    const char *vg = static_cast<const char *>(a.v_layer) + (int64_t)g * kD * 2;
-    // Q tiles: row t of head h0 + qh sits at q[(q0 + r0 + t) * H + h0 + qh]
-    {
-      const char *qb = static_cast<const char *>(a.q);
-      for (int qh = 0; qh < NQ; ++qh) {
-        const uint32_t qs = sbase + kOffQ + qh * kTile;
-        // 128 rows x 16 chunks = 2048 copies over 128 threads: 16 each, two rows per warp pass
-#pragma unroll 4
-        for (int j = 0; j < 16; ++j) {
-          const int t = j * 8 + lw * 2 + half;  // row within the tile
-          const bool v = (int64_t)t < rows_here;
-          const char *src = v ? qb + (((q0 + r0 + t) * a.H + h0 + qh) * kD) * 2 + c * 16 : qb;
-          tc::cp_async16(qs + tc::sw128_chunk_offset(t, c, kBlk), src, v ? 16u : 0u);
-        }
-      }
-      tc::cp_async_arrive_noinc(q_full);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, NQ * kTile);
+      for (int qh = 0; qh < NQ; ++qh)
+        for (int hf = 0; hf < 2; ++hf)
+          tc::tma_load_2d(sbase + kOffQ + qh * kTile + hf * kBlk, &qmap, (h0 + qh) * kD + hf * 64,
+                          (int)(q0 + r0), q_full);
     }
-    // K / V tiles
-    int64_t nxt = -1;
-    if (nkv > 0 && lw * 32 + lane < key_end) nxt = __ldg(row + lw * 32 + lane);
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
       const int64_t k0 = (int64_t)j * kKeys;
-      int64_t my = nxt;  // slot of key k0 + lw*32 + lane
-      {
-        const int64_t kn = k0 + kKeys + lw * 32 + lane;
-        nxt = (j + 1 < nkv && kn < key_end) ? (int64_t)__ldg(row + kn) : -1;
+      // keys k0 + 4 * lane + i: slot, validity, and whether 16-key groups are page runs
+      int sl[4];
+      bool vd[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t kk = k0 + 4 * lane + i;
+        vd[i] = kk < key_end;
+        sl[i] = vd[i] ? __ldg(row + kk) : -1;
+        if (vd[i] && (sl[i] < 0 || (int64_t)sl[i] >= a.size)) {
+          raise_error(a.err, ASTR_DEVERR_SLOT);
+          vd[i] = false;
+        }
       }
-      const bool in_range = k0 + lw * 32 + lane < key_end;
-      if (my >= a.size || (my < 0 && in_range)) {
-        raise_error(a.err, ASTR_DEVERR_SLOT);
-        my = -1;
+      const bool run4 = vd[0] && vd[1] && vd[2] && vd[3] && sl[1] == sl[0] + 1 &&
+                        sl[2] == sl[1] + 1 && sl[3] == sl[2] + 1;
+      const int next0 = __shfl_down_sync(0xffffffffu, sl[0], 1);
+      const bool link = ((lane & 3) == 3) || (next0 == sl[3] + 1);
+      const unsigned bal = __ballot_sync(0xffffffffu, run4 && link);
+      const bool group_run = ((bal >> (lane & ~3)) & 0xFu) == 0xFu;
+      for (int kvsel = 0; kvsel < 2; ++kvsel) {  // 0: K, 1: V
+        uint64_t *fullb = kvsel ? &v_full[st] : &k_full[st];
+        uint64_t *emptyb = kvsel ? &v_empty[st] : &k_empty[st];
+        int ok = 1;
+        if (lane == 0) {
+          if (j >= 2) ok = mbar_wait(emptyb, ((j >> 1) - 1) & 1, a.wait_ns, a.err);
+          if (*abort_flag) ok = 0;
+          if (ok) mbar_arrive_expect_tx(fullb, (uint32_t)__popc(bal & 0x11111111u & (bal >> 1) & (bal >> 2) & (bal >> 3)) * 4096u);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t dst = sbase + (kvsel ? kOffV : kOffK) + st * kTile;
+        if (group_run) {
+          if ((lane & 3) == 0) {
+            const void *m16 = kvsel ? (const void *)&v16 : (const void *)&k16;
+            if constexpr (MC) {
+              // the two CTAs stage the same keys: each issues every other 16-key run for both
+              if (((lane >> 2) & 1) == (int)crank)
+                for (int hf = 0; hf < 2; ++hf)
+                  tc::tma_load_2d_multicast(dst + hf * kBlk + (4 * lane) * 128, m16, col0 + hf * 64,
+                                            a.layer_row0 + sl[0], fullb, (uint16_t)3);
+            } else {
+              for (int hf = 0; hf < 2; ++hf)
+                tc::tma_load_2d(dst + hf * kBlk + (4 * lane) * 128, m16, col0 + hf * 64,
+                                a.layer_row0 + sl[0], fullb);
+            }
+          }
+        } else {
+          const char *base = static_cast<const char *>(kvsel ? a.v_layer : a.k_layer) + (int64_t)col0 * 2;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int t = 4 * lane + i;
+            const char *src = base + (vd[i] ? (int64_t)sl[i] * rowb_kv : 0);
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+              tc::cp_async16(dst + tc::sw128_chunk_offset(t, cc, kBlk), src + cc * 16, vd[i] ? 16u : 0u);
+          }
+        }
+        tc::cp_async_arrive_noinc(fullb);
       }
-      // K
-      int ok = 1;
-      if (lane == 0) {
-        if (j >= 2) ok = mbar_wait(&k_empty[st], ((j >> 1) - 1) & 1, a.wait_ns, a.err);
-        if (*abort_flag) ok = 0;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
-      const uint32_t kst = sbase + kOffK + st * kTile;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int tl = i * 2 + half;
-        const int t = lw * 32 + tl;
-        const int64_t s = __shfl_sync(0xffffffffu, my, tl);
-        const bool v = s >= 0;
-        tc::cp_async16(kst + tc::sw128_chunk_offset(t, c, kBlk), kg + (v ? s * rowb_kv + c * 16 : 0),
-                       v ? 16u : 0u);
-      }
-      tc::cp_async_arrive_noinc(&k_full[st]);
-      // V
-      ok = 1;
-      if (lane == 0) {
-        if (j >= 2) ok = mbar_wait(&v_empty[st], ((j >> 1) - 1) & 1, a.wait_ns, a.err);
-        if (*abort_flag) ok = 0;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
-      const uint32_t vst = sbase + kOffV + st * kTile;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int tl = i * 2 + half;
-        const int t = lw * 32 + tl;
-        const int64_t s = __shfl_sync(0xffffffffu, my, tl);
-        const bool v = s >= 0;
-        tc::cp_async16(vst + tc::sw128_chunk_offset(t, c, kBlk), vg + (v ? s * rowb_kv + c * 16 : 0),
-                       v ? 16u : 0u);
-      }
-      tc::cp_async_arrive_noinc(&v_full[st]);
+      if (*abort_flag) break;
     }
-    tc::cp_async_wait_all();
   } else {
-    // ============================== MMA issuer (one lane) =====================================
-    if (lane == 0) {
+    // ===================== MMA issuers: lane 0 of warp 17 + hh issues head hh ==================
+    // A tcgen05.mma holds its issuing thread for about as long as it occupies the tensor pipe,
+    // so each head gets its own issuer: head 0's P.V and next S go in as soon as its P is
+    // ready, while head 1's issuer may still be blocked feeding the pipe. Commits track the
+    // issuing thread, so the K/V stage releases and the drain take one arrival per head.
+    const int hh = warp - 17;
+    if (lane == 0 && hh < NQ) {
       bool ok = mbar_wait(q_full, 0, a.wait_ns, a.err);
-      auto qk = [&](int hh, int j) {
+      auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (*abort_flag || !mbar_wait(bar, parity, a.wait_ns, a.err)) return false;
+        tc::fence_after_sync();
+        tc::fence_proxy_async_smem();  // rows that came by cp.async (generic proxy)
+        return true;
+      };
+      auto qk = [&](int j) {
         const uint32_t qaddr = sbase + kOffQ + hh * kTile;
         const uint32_t kaddr = sbase + kOffK + (j & 1) * kTile;
 #pragma unroll
@@ -381,43 +424,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a
           tc::mma_ss(tmem + hh * 128, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(&s_full[hh]);
-      };
-      auto pv = [&](int hh, int j) {
-        const uint32_t vaddr = sbase + kOffV + (j & 1) * kTile;
-#pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks) {
-          const uint64_t bd = tc::desc_sw128(vaddr + ks * 2048, kBlk, 1024);
-          tc::mma_ts(tmem + 256 + hh * 128, tmem + hh * 128 + ks * 8, bd, kIdescPV,
-                     (j > 0 || ks > 0) ? 1u : 0u);
-        }
-      };
-      auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-        if (*abort_flag || !mbar_wait(bar, parity, a.wait_ns, a.err)) return false;
-        tc::fence_after_sync();
-        tc::fence_proxy_async_smem();
-        return true;
+        if constexpr (MC)
+          tc::mma_commit_multicast(&k_empty[j & 1], (uint16_t)3);
+        else
+          tc::mma_commit(&k_empty[j & 1]);
       };
       if (ok) {
         tc::fence_after_sync();
-        tc::fence_proxy_async_smem();
-        ok = nkv == 0 || wait(&k_full[0], 0);
-        if (ok && nkv > 0) {
-          for (int hh = 0; hh < NQ; ++hh) qk(hh, 0);
-          tc::mma_commit(&k_empty[0]);
-        }
+        ok = wait(&k_full[0], 0);
+        if (ok) qk(0);
         for (int j = 0; j < nkv && ok; ++j) {
-          const bool more = j + 1 < nkv;
-          for (int hh = 0; hh < NQ && ok; ++hh) {
-            if (!wait(&p_full[hh], j & 1)) { ok = false; break; }
-            if (hh == 0 && !wait(&v_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
-            pv(hh, j);
-            if (!more) tc::mma_commit(&o_done[hh]);
-            if (hh == NQ - 1) tc::mma_commit(&v_empty[j & 1]);
-            if (more) {
-              if (hh == 0 && !wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) { ok = false; break; }
-              qk(hh, j + 1);
-              if (hh == NQ - 1) tc::mma_commit(&k_empty[(j + 1) & 1]);
+          if (!wait(&p_full[hh], j & 1) || !wait(&v_full[j & 1], (j >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vaddr = sbase + kOffV + (j & 1) * kTile;
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint64_t bd = tc::desc_sw128(vaddr + ks * 2048, kBlk, 1024);
+            tc::mma_ts(tmem + 256 + hh * 128, tmem + hh * 128 + (ks >> 2) * 64 + (ks & 3) * 8, bd,
+                       kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          if constexpr (MC)
+            tc::mma_commit_multicast(&v_empty[j & 1], (uint16_t)3);
+          else
+            tc::mma_commit(&v_empty[j & 1]);
+          if (j + 1 == nkv) {
+            tc::mma_commit(&o_done[hh]);
+          } else {
+            if (!wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
+              ok = false;
+              break;
             }
+            qk(j + 1);
           }
         }
       }
@@ -430,29 +469,61 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PreArgs a
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 12) {
+  if (warp == 17) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
   }
+  if constexpr (MC) {
+    // both CTAs have issued their last copies and commits; after an abort, give the peer's
+    // copies into this CTA's stages a bounded moment to land before the block goes away
+    tc::cluster_sync();
+    if (*abort_flag) {
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 50000) {
+      }
+    }
+  }
 }
 
-template <int NQ>
-cudaError_t run_nq(const PreArgs &a, int64_t grid, cudaStream_t s) {
-  auto k = prefill_tc_kernel<NQ>;
+struct Maps {
+  CUtensorMap q, k16, v16;
+};
+
+template <int NQ, bool MC>
+cudaError_t run_nq(const PreArgs &a, const Maps &m, int64_t grid, cudaStream_t s) {
+  auto k = prefill_tc_kernel<NQ, MC>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a);
-  return cudaGetLastError();
+  if (grid <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = MC ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, m.q, m.k16, m.v16);
 }
 
 }  // namespace
 
 bool tc_prefill_supported(int dtype, int head_dim, int group, int q_tile_rows) {
   return dtype == ASTR_BF16 && head_dim == kD && q_tile_rows == kRows && group >= 1;
+}
+
+bool tc_prefill_fits(const astr_kv_cache &kv) {
+  // TMA row coordinates are 32-bit
+  return (int64_t)kv.n_layers * kv.size < (int64_t(1) << 31) && kv.n_tokens >= 1 &&
+         kv.n_tokens < (int64_t(1) << 31);
 }
 
 cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const void *q, void *out,
@@ -481,9 +552,21 @@ cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const v
   a.B = kv.batch;
   a.num_tiles = kv.num_q_tiles;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kv.head_dim));
+  a.layer_row0 = (int32_t)((int64_t)layer_id * kv.size);
+  a.total_rows = (int32_t)((int64_t)kv.n_layers * kv.size);
+  Maps m;
+  const uint64_t rows = (uint64_t)kv.n_layers * kv.size;
+  const uint64_t cols = (uint64_t)kv.n_kv_heads * kv.head_dim;
+  if (!encode_map_bf16_2d(&m.q, q, (uint64_t)kv.n_tokens, (uint64_t)n_heads * kv.head_dim, 64, kRows) ||
+      !encode_map_bf16_2d(&m.k16, kv.k_buffer, rows, cols, 64, 16) ||
+      !encode_map_bf16_2d(&m.v16, kv.v_buffer, rows, cols, 64, 16))
+    return cudaErrorInvalidValue;
   const int G = n_heads / kv.n_kv_heads;
-  if (G % 2 == 0) return run_nq<2>(a, (int64_t)kv.num_q_tiles * (n_heads / 2), stream);
-  return run_nq<1>(a, (int64_t)kv.num_q_tiles * n_heads, stream);
+  // blocks (2c, 2c+1) are head pairs 2c, 2c+1 of one KV group on the same Q tile when the
+  // group holds an even number of pairs: they form a cluster and share every K/V tile
+  if (G % 4 == 0) return run_nq<2, true>(a, m, (int64_t)kv.num_q_tiles * (n_heads / 2), stream);
+  if (G % 2 == 0) return run_nq<2, false>(a, m, (int64_t)kv.num_q_tiles * (n_heads / 2), stream);
+  return run_nq<1, false>(a, m, (int64_t)kv.num_q_tiles * n_heads, stream);
 }
 
 }  // namespace astr
