@@ -8,23 +8,21 @@
 // with prefix P sits at P + i).
 //
 // One block computes a 128-row Q tile for NQ = 2 query heads of the same KV group (1 when
-// the group has a single head), so every K/V tile it stages feeds two heads; when the group
-// has two or more such pairs, the blocks of two pairs form a cluster and each K/V box is
-// fetched once and multicast into both blocks' shared memory:
-//  * warp 16 streams the two Q tiles once and then 128-key K and V tiles (two stages each,
+// the group has a single head), so every K/V tile it stages feeds two heads:
+//  * warp 8 streams the two Q tiles once and then 128-key K and V tiles (two stages each,
 //    released separately) into the 128-byte-swizzled layout: one TMA tensor copy of a 16-row
 //    box per run of 16 keys whose slots are consecutive (a page; destinations 2 KB aligned),
-//    16-byte cp.async copies for keys outside such runs, zero-filled past the request;
-//  * warp 17 allocates all 512 TMEM columns -- S0 | S1 | O0 | O1, 128 each -- and warps 17
-//    and 18 each issue one head's MMAs, S_h = Q_h K^T (M = N = K = 128) and O_h += P_h V
-//    (P_h read from TMEM where the softmax wrote it over S_h, V an MN-major operand); with one
-//    issuer per head the tensor core works on one head while the other head's softmax runs;
-//  * warps 0-7 and 8-15 are the softmax of head 0 and head 1, two threads per row (64 scores
-//    each, partial maxima exchanged through shared memory): a pass for the row max, the
-//    reference max raised only when the row max exceeds it by 2^8 (the O row is then rescaled
-//    in TMEM; the commit that published S also covers the previous P.V), a pass writing exp2
-//    of the scaled scores as bf16 P over the thread's own half of S, and the epilogue that
-//    normalises O.
+//    16-byte cp.async copies for keys outside such runs, zero-filled past the request; the
+//    page-table entries of a tile are read while the previous tile's copies are issued;
+//  * warp 9 allocates all 512 TMEM columns -- S0 | S1 | O0 | O1, 128 each -- and one of its
+//    threads issues the MMAs, S_h = Q_h K^T (M = N = K = 128) and O_h += P_h V (P_h read
+//    from TMEM where the softmax wrote it over S_h, V an MN-major operand), head by head, so
+//    that the tensor core works on one head while the other head's softmax runs;
+//  * warps 0-3 and 4-7 are the softmax of head 0 and head 1, one thread per row holding all
+//    128 scores of a tile in registers: the row max, the reference max raised only when the
+//    row max exceeds it by 2^8 (the O row is then rescaled in TMEM; the commit that published
+//    S also covers the previous P.V), exp2 of the scaled scores written as bf16 P over the
+//    first 64 columns of S, and the epilogue that normalises O.
 // KV tiles beyond the diagonal of the tile are skipped; the mask is applied only to tiles
 // that cross the diagonal or the end of the request. All waits are bounded.
 #include <math.h>
@@ -43,14 +41,13 @@ constexpr int kKeys = 128;                 // keys per KV tile (N of S, K of P.V
 constexpr int kD = 128;
 constexpr int kTile = kRows * kD * 2;      // 32 KB: one Q, K or V tile
 constexpr int kBlk = kRows * 128;          // 16 KB: one 64-element half
-constexpr int kThreads = 608;              // 16 softmax + 1 loader + 2 MMA warps
+constexpr int kThreads = 320;              // 8 softmax + 1 loader + 1 MMA warp
 constexpr float kLazyRescale = 8.0f;
 
 constexpr int kOffQ = 0;                   // 2 Q tiles
 constexpr int kOffK = kOffQ + 2 * kTile;   // 2 K stages
 constexpr int kOffV = kOffK + 2 * kTile;   // 2 V stages
-constexpr int kOffRed = kOffV + 2 * kTile;   // [2 heads][3 bufs][2 halves][128] f32
-constexpr int kOffBar = kOffRed + 2 * 3 * 2 * 128 * 4;
+constexpr int kOffBar = kOffV + 2 * kTile;
 constexpr int kOffMisc = kOffBar + 32 * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
 
@@ -80,18 +77,7 @@ struct PreArgs {
   float scale_log2;
 };
 
-__device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
-template <int NQ, bool MC>
+template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PreArgs a, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap k16, const __grid_constant__ CUtensorMap v16) {
@@ -157,93 +143,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {  // 32 loader lanes (cp.async) + one expect-tx arrival (TMA)
       mbar_init(&k_full[i], 33);
       mbar_init(&v_full[i], 33);
-      mbar_init(&k_empty[i], NQ * (MC ? 2 : 1));  // one commit per head issuer, per CTA
-      mbar_init(&v_empty[i], NQ * (MC ? 2 : 1));
+      mbar_init(&k_empty[i], 1);  // MMA commits
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 256);
+      mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(drain, NQ);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 17) {
+  if (warp == 9) {
     tc::tmem_alloc(tmem_slot, 512);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  if constexpr (MC)
-    tc::cluster_sync();  // both CTAs' barriers exist before either copies or commits into them
-  else
-    __syncthreads();
+  __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t crank = MC ? tc::cluster_ctarank() : 0;
 
-  if (warp < 16) {
-    // ============ softmax: head h = warp / 8, column half cb = (warp / 4) & 1, row = lane quarter
-    // Two threads own a row: each reads 64 of its 128 scores, they exchange their partial maxima
-    // through shared memory once per tile, and each writes its 64 P values into the first 32
-    // columns of its own half of S, so neither overwrites scores the other still has to read.
-    const int h = warp >> 3;
-    const int cb = (warp >> 2) & 1;
+  if (warp < 8) {
+    // ============ softmax: head h = warp / 4, one thread per row, all 128 scores in registers
+    const int h = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     if (h < NQ) {
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-      const uint32_t tS = tmem + h * 128 + cb * 64 + lane_base;
-      const uint32_t tO = tmem + 256 + h * 128 + cb * 64 + lane_base;
-      // [3 buffers][2 halves][128 rows]: tile maxima alternate between 0 and 1, 2 is for the sums
-      float *xred = reinterpret_cast<float *>(smem + kOffRed) + h * 3 * 2 * 128;
+      const uint32_t tS = tmem + h * 128 + lane_base;
+      const uint32_t tO = tmem + 256 + h * 128 + lane_base;
       const int64_t pos = Pb + r0 + r;  // absolute position of this row
       const int64_t pos_min = Pb + r0;
+      const int64_t lim_row = (pos + 1 < Kb ? pos + 1 : Kb);  // keys [0, lim_row) are visible
       float m = -INFINITY, l = 0.f;
       bool aborted = false;
-      const int bar_id = 1 + h;
       for (int j = 0; j < nkv; ++j) {
-        const bool ok = mbar_wait(&s_full[h], j & 1, a.wait_ns, a.err);
-        const int64_t k0 = (int64_t)j * kKeys + cb * 64;  // first key of my half
-        const bool masked = ((int64_t)j * kKeys + kKeys - 1 > pos_min) || ((int64_t)j * kKeys + kKeys > Kb);
-        int nvalid = 64;
-        if (masked) {
-          const int64_t lim = (pos + 1 < Kb ? pos + 1 : Kb) - k0;
-          nvalid = lim < 0 ? 0 : (lim > 64 ? 64 : (int)lim);
-        }
-        float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
-        if (ok) {
-          tc::fence_after_sync();
-          uint32_t buf[2][32];
-          tc::tmem_ld32(tS, buf[0]);
-          tc::tmem_ld32(tS + 32, buf[1]);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t *sv = buf[c];
-            if (masked) {
-#pragma unroll
-              for (int k = 0; k < 32; ++k)
-                if (c * 32 + k >= nvalid) sv[k] = 0xFF800000u;  // -inf
-            }
-#pragma unroll
-            for (int k = 0; k < 32; k += 8) {
-              mxa = fmax3(mxa, __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
-              mxb = fmax3(mxb, __uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3]));
-              mxc = fmax3(mxc, __uint_as_float(sv[k + 4]), __uint_as_float(sv[k + 5]));
-              mxd = fmax3(mxd, __uint_as_float(sv[k + 6]), __uint_as_float(sv[k + 7]));
-            }
-          }
-          xred[((j & 1) * 2 + cb) * 128 + r] = fmax3(mxa, mxb, fmaxf(mxc, mxd));
-        }
-        if (bar_any(bar_id, 256, !ok)) {  // also publishes the partial maxima
+        if (!mbar_wait(&s_full[h], j & 1, a.wait_ns, a.err)) {
           aborted = true;
           break;
         }
-        const float mx = fmaxf(xred[((j & 1) * 2 + 0) * 128 + r], xred[((j & 1) * 2 + 1) * 128 + r]) * a.scale_log2;
+        tc::fence_after_sync();
+        uint32_t sv[128];
+        tc::tmem_ld32(tS, sv);
+        tc::tmem_ld32(tS + 32, sv + 32);
+        tc::tmem_ld32(tS + 64, sv + 64);
+        tc::tmem_ld32(tS + 96, sv + 96);
+        tc::tmem_ld_wait();
+        // only tiles crossing this tile's diagonal or the end of the request carry masked keys
+        if ((int64_t)j * kKeys + kKeys - 1 > pos_min || (int64_t)j * kKeys + kKeys > Kb) {
+          const int64_t lim = lim_row - (int64_t)j * kKeys;
+          const int nvalid = lim < 0 ? 0 : (lim > kKeys ? kKeys : (int)lim);
+#pragma unroll
+          for (int k = 0; k < kKeys; ++k)
+            if (k >= nvalid) sv[k] = 0xFF800000u;  // -inf
+        }
+        float mxa = -INFINITY, mxb = -INFINITY, mxc = -INFINITY, mxd = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kKeys; k += 8) {
+          mxa = fmax3(mxa, __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
+          mxb = fmax3(mxb, __uint_as_float(sv[k + 2]), __uint_as_float(sv[k + 3]));
+          mxc = fmax3(mxc, __uint_as_float(sv[k + 4]), __uint_as_float(sv[k + 5]));
+          mxd = fmax3(mxd, __uint_as_float(sv[k + 6]), __uint_as_float(sv[k + 7]));
+        }
+        const float mx = fmax3(mxa, mxb, fmaxf(mxc, mxd)) * a.scale_log2;
         const float m_new = (mx > m + kLazyRescale) ? mx : m;
         const float alpha = ex2_approx(m - m_new);
-        if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, m_new != m);
+        l *= alpha;
+        m = m_new;
+        // P = exp2(score * scale - m) in bf16 over the first 64 columns of S (the row's
+        // scores are all in registers, so nothing still to be read is overwritten)
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+        const float2 nm2 = make_float2(-m, -m);
+        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const float2 x = ffma2(make_float2(__uint_as_float(sv[32 * c + k]), __uint_as_float(sv[32 * c + k + 1])),
+                                   sc2, nm2);
+            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);  // ex2(-inf) = 0
+            sum2[(k >> 1) & 3] = fadd2(sum2[(k >> 1) & 3], make_float2(p0, p1));
+            pk[k >> 1] = pack_bf16x2_rn(p0, p1);
+          }
+          tc::tmem_st16(tS + c * 16, pk);
+        }
+        const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
+        l += (s01.x + s01.y) + (s23.x + s23.y);
+        if (rescale) {
           // the commit behind s_full also covers P.V of the previous tile: O is settled
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
             tc::tmem_ld32(tO + c * 32, o);
             tc::tmem_ld_wait();
@@ -252,56 +242,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tmem_st16(tO + c * 32, o);
             tc::tmem_st16(tO + c * 32 + 16, o + 16);
           }
-          tc::tmem_st_wait();
         }
-        l *= alpha;
-        m = m_new;
-        // P = exp2(score * scale - m) in bf16, into columns [0, 32) of my half of S
-        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
-        const float2 nm2 = make_float2(-m, -m);
-        float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
-        {
-          uint32_t buf[2][32];
-          tc::tmem_ld32(tS, buf[0]);
-          tc::tmem_ld32(tS + 32, buf[1]);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t *sv = buf[c];
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float2 x = ffma2(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), sc2, nm2);
-              float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-              if (masked) {
-                if (c * 32 + k >= nvalid) p0 = 0.f;
-                if (c * 32 + k + 1 >= nvalid) p1 = 0.f;
-              }
-              sum2[(k >> 1) & 3] = fadd2(sum2[(k >> 1) & 3], make_float2(p0, p1));
-              pk[k >> 1] = pack_bf16x2_rn(p0, p1);
-            }
-            tc::tmem_st16(tS + c * 16, pk);
-          }
-        }
-        const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
-        l += (s01.x + s01.y) + (s23.x + s23.y);
         tc::tmem_st_wait();
         tc::fence_before_sync();
         mbar_arrive(&p_full[h]);
       }
       if (!aborted && nkv > 0) {
-        const bool ok = mbar_wait(&o_done[h], 0, a.wait_ns, a.err);
-        xred[(2 * 2 + cb) * 128 + r] = l;  // both partial sums of the row
-        if (bar_any(bar_id, 256, !ok)) {
+        if (!mbar_wait(&o_done[h], 0, a.wait_ns, a.err)) {
           aborted = true;
         } else {
           tc::fence_after_sync();
-          const float inv = 1.f / (xred[4 * 128 + r] + xred[5 * 128 + r]);
-          uint16_t *orow = static_cast<uint16_t *>(a.out) + ((q0 + r0 + r) * a.H + h0 + h) * kD + cb * 64;
+          const float inv = 1.f / l;
+          uint16_t *orow = static_cast<uint16_t *>(a.out) + ((q0 + r0 + r) * a.H + h0 + h) * kD;
           const bool write = (int64_t)r < rows_here;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
             tc::tmem_ld32(tO + c * 32, o);
             tc::tmem_ld_wait();
@@ -321,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (aborted) *abort_flag = 1;
     }
-  } else if (warp == 16) {
+  } else if (warp == 8) {
     // ============================== TMA loader (one warp) ======================================
     const int col0 = g * kD;  // this KV head's columns in the [rows, Hk * D] view
     const int64_t rowb_kv = (int64_t)a.Hk * kD * 2;
@@ -332,22 +287,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_2d(sbase + kOffQ + qh * kTile + hf * kBlk, &qmap, (h0 + qh) * kD + hf * 64,
                           (int)(q0 + r0), q_full);
     }
+    // keys k0 + 4 * lane + i of a tile: their slots are read one tile ahead of the copies
+    auto fetch_slots = [&](int j, int (&sl)[4]) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t kk = (int64_t)j * kKeys + 4 * lane + i;
+        sl[i] = kk < key_end ? __ldg(row + kk) : -1;
+      }
+    };
+    int sl_next[4];
+    fetch_slots(0, sl_next);
     for (int j = 0; j < nkv; ++j) {
       const int st = j & 1;
-      const int64_t k0 = (int64_t)j * kKeys;
-      // keys k0 + 4 * lane + i: slot, validity, and whether 16-key groups are page runs
       int sl[4];
       bool vd[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int64_t kk = k0 + 4 * lane + i;
-        vd[i] = kk < key_end;
-        sl[i] = vd[i] ? __ldg(row + kk) : -1;
+        sl[i] = sl_next[i];
+        vd[i] = (int64_t)j * kKeys + 4 * lane + i < key_end;
         if (vd[i] && (sl[i] < 0 || (int64_t)sl[i] >= a.size)) {
           raise_error(a.err, ASTR_DEVERR_SLOT);
           vd[i] = false;
         }
       }
+      if (j + 1 < nkv) fetch_slots(j + 1, sl_next);
+      // whether each 16-key group is a run of consecutive slots (one page)
       const bool run4 = vd[0] && vd[1] && vd[2] && vd[3] && sl[1] == sl[0] + 1 &&
                         sl[2] == sl[1] + 1 && sl[3] == sl[2] + 1;
       const int next0 = __shfl_down_sync(0xffffffffu, sl[0], 1);
@@ -372,17 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (group_run) {
           if ((lane & 3) == 0) {
             const void *m16 = kvsel ? (const void *)&v16 : (const void *)&k16;
-            if constexpr (MC) {
-              // the two CTAs stage the same keys: each issues every other 16-key run for both
-              if (((lane >> 2) & 1) == (int)crank)
-                for (int hf = 0; hf < 2; ++hf)
-                  tc::tma_load_2d_multicast(dst + hf * kBlk + (4 * lane) * 128, m16, col0 + hf * 64,
-                                            a.layer_row0 + sl[0], fullb, (uint16_t)3);
-            } else {
-              for (int hf = 0; hf < 2; ++hf)
-                tc::tma_load_2d(dst + hf * kBlk + (4 * lane) * 128, m16, col0 + hf * 64,
-                                a.layer_row0 + sl[0], fullb);
-            }
+            for (int hf = 0; hf < 2; ++hf)
+              tc::tma_load_2d(dst + hf * kBlk + (4 * lane) * 128, m16, col0 + hf * 64,
+                              a.layer_row0 + sl[0], fullb);
           }
         } else {
           const char *base = static_cast<const char *>(kvsel ? a.v_layer : a.k_layer) + (int64_t)col0 * 2;
@@ -400,13 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) break;
     }
   } else {
-    // ===================== MMA issuers: lane 0 of warp 17 + hh issues head hh ==================
-    // A tcgen05.mma holds its issuing thread for about as long as it occupies the tensor pipe,
-    // so each head gets its own issuer: head 0's P.V and next S go in as soon as its P is
-    // ready, while head 1's issuer may still be blocked feeding the pipe. Commits track the
-    // issuing thread, so the K/V stage releases and the drain take one arrival per head.
-    const int hh = warp - 17;
-    if (lane == 0 && hh < NQ) {
+    // ===================== MMA issuer: lane 0 of warp 9 ========================================
+    // A tcgen05.mma holds its issuing thread for about as long as it occupies the tensor pipe.
+    // One thread issues both heads in a fixed order -- per KV tile, head 0's P.V and next S,
+    // then head 1's -- so each head's MMAs run as a block: head 1's S lands one block after
+    // head 0's, and from then on one head's softmax runs while the tensor core works for the
+    // other, instead of both softmaxes contending for the exp2 unit at once.
+    if (lane == 0) {
       bool ok = mbar_wait(q_full, 0, a.wait_ns, a.err);
       auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
         if (*abort_flag || !mbar_wait(bar, parity, a.wait_ns, a.err)) return false;
@@ -414,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async_smem();  // rows that came by cp.async (generic proxy)
         return true;
       };
-      auto qk = [&](int j) {
+      auto qk = [&](int hh, int j) {
         const uint32_t qaddr = sbase + kOffQ + hh * kTile;
         const uint32_t kaddr = sbase + kOffK + (j & 1) * kTile;
 #pragma unroll
@@ -424,40 +380,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_ss(tmem + hh * 128, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
         }
         tc::mma_commit(&s_full[hh]);
-        if constexpr (MC)
-          tc::mma_commit_multicast(&k_empty[j & 1], (uint16_t)3);
-        else
-          tc::mma_commit(&k_empty[j & 1]);
       };
       if (ok) {
         tc::fence_after_sync();
         ok = wait(&k_full[0], 0);
-        if (ok) qk(0);
+        if (ok) {
+          for (int hh = 0; hh < NQ; ++hh) qk(hh, 0);
+          tc::mma_commit(&k_empty[0]);
+        }
         for (int j = 0; j < nkv && ok; ++j) {
-          if (!wait(&p_full[hh], j & 1) || !wait(&v_full[j & 1], (j >> 1) & 1)) {
+          if (!wait(&v_full[j & 1], (j >> 1) & 1)) {
             ok = false;
             break;
           }
           const uint32_t vaddr = sbase + kOffV + (j & 1) * kTile;
-#pragma unroll
-          for (int ks = 0; ks < kKeys / 16; ++ks) {
-            const uint64_t bd = tc::desc_sw128(vaddr + ks * 2048, kBlk, 1024);
-            tc::mma_ts(tmem + 256 + hh * 128, tmem + hh * 128 + (ks >> 2) * 64 + (ks & 3) * 8, bd,
-                       kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
-          }
-          if constexpr (MC)
-            tc::mma_commit_multicast(&v_empty[j & 1], (uint16_t)3);
-          else
-            tc::mma_commit(&v_empty[j & 1]);
-          if (j + 1 == nkv) {
-            tc::mma_commit(&o_done[hh]);
-          } else {
-            if (!wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
+          for (int hh = 0; hh < NQ && ok; ++hh) {
+            if (!wait(&p_full[hh], j & 1)) {
               ok = false;
               break;
             }
-            qk(j + 1);
+#pragma unroll
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              const uint64_t bd = tc::desc_sw128(vaddr + ks * 2048, kBlk, 1024);
+              tc::mma_ts(tmem + 256 + hh * 128, tmem + hh * 128 + ks * 8, bd, kIdescPV,
+                         (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            if (j + 1 == nkv) {
+              tc::mma_commit(&o_done[hh]);
+            } else {
+              if (hh == 0 && !wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
+                ok = false;
+                break;
+              }
+              qk(hh, j + 1);  // overwrites S_hh: issued after the P.V that reads P_hh from it
+            }
           }
+          if (!ok) break;
+          tc::mma_commit(&v_empty[j & 1]);
+          if (j + 1 < nkv) tc::mma_commit(&k_empty[(j + 1) & 1]);
         }
       }
       if (!ok) *abort_flag = 1;
@@ -469,19 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 17) {
+  if (warp == 9) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 512);
-  }
-  if constexpr (MC) {
-    // both CTAs have issued their last copies and commits; after an abort, give the peer's
-    // copies into this CTA's stages a bounded moment to land before the block goes away
-    tc::cluster_sync();
-    if (*abort_flag) {
-      const uint64_t t0 = global_timer_ns();
-      while (global_timer_ns() - t0 < 50000) {
-      }
-    }
   }
 }
 
@@ -489,9 +439,9 @@ struct Maps {
   CUtensorMap q, k16, v16;
 };
 
-template <int NQ, bool MC>
+template <int NQ>
 cudaError_t run_nq(const PreArgs &a, const Maps &m, int64_t grid, cudaStream_t s) {
-  auto k = prefill_tc_kernel<NQ, MC>;
+  auto k = prefill_tc_kernel<NQ>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -499,19 +449,8 @@ cudaError_t run_nq(const PreArgs &a, const Maps &m, int64_t grid, cudaStream_t s
     attr_set = true;
   }
   if (grid <= 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = MC ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, m.q, m.k16, m.v16);
+  k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, m.q, m.k16, m.v16);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -562,11 +501,8 @@ cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const v
       !encode_map_bf16_2d(&m.v16, kv.v_buffer, rows, cols, 64, 16))
     return cudaErrorInvalidValue;
   const int G = n_heads / kv.n_kv_heads;
-  // blocks (2c, 2c+1) are head pairs 2c, 2c+1 of one KV group on the same Q tile when the
-  // group holds an even number of pairs: they form a cluster and share every K/V tile
-  if (G % 4 == 0) return run_nq<2, true>(a, m, (int64_t)kv.num_q_tiles * (n_heads / 2), stream);
-  if (G % 2 == 0) return run_nq<2, false>(a, m, (int64_t)kv.num_q_tiles * (n_heads / 2), stream);
-  return run_nq<1, false>(a, m, (int64_t)kv.num_q_tiles * n_heads, stream);
+  if (G % 2 == 0) return run_nq<2>(a, m, (int64_t)kv.num_q_tiles * (n_heads / 2), stream);
+  return run_nq<1>(a, m, (int64_t)kv.num_q_tiles * n_heads, stream);
 }
 
 }  // namespace astr

@@ -155,33 +155,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_saddr, const void *map,
       : "memory");
 }
 
-// ---- clusters ------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// every thread of every CTA of the cluster arrives, then waits for all the others
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// the 2-D box lands at the same shared-memory offset in every CTA of `mask`, and completes
-// transaction bytes on the mbarrier at the same offset in each of them
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst_saddr, const void *map, int x, int y,
-                                                      uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
-          dst_saddr),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-// like mma_commit, arriving on the mbarrier at this offset in every CTA of `mask`
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
+// warms L2 with the 2-D box at (x, y) of `map`; no shared memory or barrier involved
+__device__ __forceinline__ void tma_prefetch_2d(const void *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 // ---- Ampere-style async copies (16 bytes, zero-filled when src_bytes = 0) -----------------
