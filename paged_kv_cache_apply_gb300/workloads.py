@@ -105,14 +105,26 @@ def prefix_sum(lengths) -> np.ndarray:
     return out.astype(np.int32)
 
 
-def q_tiles(q_lens, tile_rows: int = Q_TILE_ROWS):
-    """``q_tile_to_batch`` / ``q_tile_to_index`` for ``tile_rows``-row Q tiles per request."""
-    tb, ti = [], []
+def q_tiles(q_lens, kv_lens=None, tile_rows: int = Q_TILE_ROWS):
+    """``q_tile_to_batch`` / ``q_tile_to_index`` for ``tile_rows``-row Q tiles per request.
+
+    Without ``kv_lens`` the tiles are listed request by request. With them, the tiles are
+    listed by the number of 128-key KV tiles each one visits under the causal mask, cheapest
+    first (ties in request order). The tensor-core prefill starts its blocks from the end of
+    the list, so the costliest tiles are scheduled first and the SMs finish together. Any
+    order gives the same result.
+    """
+    tb, ti, cost = [], [], []
     for b, ql in enumerate(q_lens):
-        for t in range((int(ql) + tile_rows - 1) // tile_rows):
+        ql = int(ql)
+        prefix = 0 if kv_lens is None else int(kv_lens[b]) - ql
+        for t in range((ql + tile_rows - 1) // tile_rows):
             tb.append(b)
             ti.append(t)
-    return np.asarray(tb, dtype=np.int32), np.asarray(ti, dtype=np.int32)
+            last_row = min(ql, (t + 1) * tile_rows)
+            cost.append((prefix + last_row + 127) // 128)
+    order = np.argsort(np.asarray(cost), kind="stable") if kv_lens is not None else np.arange(len(tb))
+    return (np.asarray(tb, dtype=np.int32)[order], np.asarray(ti, dtype=np.int32)[order])
 
 
 @dataclass
@@ -338,7 +350,7 @@ def config3(seed: int = SEED_BASE + 3, batch: int = 8, qmin: int = 256, qmax: in
         pool.req_to_token[rpi[b], : slots[b].size] = slots[b]
         used.append(slots[b][: kvl[b]])
     _fill_rows(pool, np.concatenate(used), seed, 10)
-    tb, ti = q_tiles(qlens)
+    tb, ti = q_tiles(qlens, kvl)
     pre = PrefillBatch(req_pool_indices=rpi, qo_indptr=prefix_sum(qlens),
                        kv_indptr=prefix_sum(kvl), q_tile_to_batch=tb, q_tile_to_index=ti,
                        q=normal_values((int(qlens.sum()), H, D), "bf16", seed, 20))
@@ -411,7 +423,7 @@ def config5(seed: int = SEED_BASE + 5, n_decode: int = 256, lmin: int = 128, lma
     dec = DecodeBatch(req_pool_indices=rows[:n_decode], seq_lens=dl, kv_indptr=prefix_sum(dl),
                       max_len=int(dl.max()), q=None, q_token_offset=0, split_chunk=0,
                       max_splits=16)
-    tb, ti = q_tiles(pl)
+    tb, ti = q_tiles(pl, pl)
     pre = PrefillBatch(req_pool_indices=rows[n_decode:], qo_indptr=prefix_sum(pl),
                        kv_indptr=prefix_sum(pl), q_tile_to_batch=tb, q_tile_to_index=ti,
                        q=None, q_token_offset=n_decode)
