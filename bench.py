@@ -377,8 +377,8 @@ def run_gpu(args):
             "decode": {"ms": round(dec_ms, 5), "GB/s": round(dec_gbs, 1),
                        "frac_hbm": round(dec_gbs / hbm, 4)},
         },
-        "roofline": {"kernel": "decode_tc_kernel, timed as the astr_decode_attention call "
-                               "(partials + LSE merge); traffic is the partial kernel's",
+        "roofline": {"kernel": "astr_decode_attention call: decode_tc_kernel partials + "
+                               "split_merge_kernel (timed together, traffic of both)",
                      "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm, 4), "traffic": traffic,
