@@ -117,6 +117,7 @@ DECODE_CASES = [
     ("f32", 4, 4, 128, 1, [7, 100, 129], 0),
     ("f32", 16, 2, 128, 16, [2, 90, 400], 96),
     ("bf16", 2, 2, 64, 1, [1, 8, 4000], 512),
+    ("bf16", 64, 4, 128, 16, [1, 129, 1000], 0),      # G = 16 on the tensor cores
 ]
 
 
@@ -142,6 +143,10 @@ PREFILL_CASES = [
     ("f32", 4, 2, 64, 16, [13, 160, 48], [13, 128, 16]),
     ("f32", 8, 1, 128, 1, [100, 37], [99, 5]),
     ("bf16", 16, 16, 128, 16, [1040, 130], [16, 130]),
+    ("bf16", 12, 4, 128, 16, [300, 77], [300, 40]),        # G = 3: one query head per block
+    ("bf16", 32, 4, 128, 16, [600, 129], [256, 129]),      # G = 8: four head pairs per group
+    ("bf16", 16, 4, 128, 1, [400, 129, 64], [400, 1, 64]),  # page 1: no page runs, all cp.async
+    ("bf16", 16, 4, 128, 16, [50, 500, 20], [0, 300, 20]),  # a request with no new rows
 ]
 
 
