@@ -7,9 +7,12 @@
 // Decode reads 512 bytes of K+V per token and KV head and does 4*G multiply-adds per byte,
 // so the block is built around the copy pipeline and keeps the arithmetic off the CUDA
 // cores. One block handles (request, chunk, KV head g) with the G query heads of the group:
-//  * warps 4-7 stream 128-token tiles of this head's K and V slices into a 3-stage ring with
-//    16-byte cp.async copies (two lanes-halves per token row, fully coalesced), writing the
-//    128-byte-swizzled operand layout directly; positions past the chunk are zero-filled;
+//  * warps 4-7 stream 128-token tiles of this head's K and V slices into a 3-stage ring in the
+//    128-byte-swizzled operand layout, 32 tokens per warp: when those are two whole pages (two
+//    runs of 16 consecutive slots) they come as four TMA boxes of 16 rows (one per 64-element
+//    half of K and of V), otherwise as 16-byte cp.async copies (two lane-halves per token row,
+//    fully coalesced) with positions past the chunk zero-filled. Which path a warp takes is
+//    uniform across it, so the copy loop stays the same straight-line code;
 //  * warp 8 allocates 64 TMEM columns and issues, per tile, S^T = K Q^T (M = 128 tokens on
 //    the TMEM lanes, N = 16 query rows of which G are the group, K = 128) into one of two
 //    S buffers, and O^T += V^T P^T (M = 128 = head_dim, N = 16, K = 128 tokens) with V read
@@ -22,10 +25,12 @@
 // Every wait is bounded; a bad slot is zero-filled and flagged; on a timeout the block stops,
 // waits for its own copies and MMAs, frees TMEM and returns.
 #include <math.h>
+#include <string.h>
 
 #include "astr_internal.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
+#include "tma_maps.h"
 
 namespace astr {
 
@@ -70,6 +75,8 @@ struct DecArgs {
   int32_t num_reqs, max_ctx;
   int32_t H, Hk, B;
   int32_t chunk, n_splits, max_splits, max_len;
+  int32_t layer_row0;  // first row of this layer in the [n_layers * size, Hk * D] tensor maps
+  int32_t use_tma;     // page runs by TMA (the maps' row coordinates fit in 32 bits)
   float scale_log2;
 };
 
@@ -133,13 +140,15 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const float (&x)[G]) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const DecArgs a, const __grid_constant__ CUtensorMap k16,
+                     const __grid_constant__ CUtensorMap v16) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-  uint64_t *full = bars;                 // [kStages] loaders -> MMA (128 arrivals)
+  uint64_t *full = bars;                 // [kStages] loaders -> MMA (128 + 4 arrivals, TMA bytes)
   uint64_t *empty = bars + kStages;      // [kStages] MMA -> loaders (commit)
   uint64_t *s_full = bars + 2 * kStages; // [2] MMA -> softmax (commit)
   uint64_t *p_full = s_full + 2;         // [2] softmax -> MMA (128 arrivals)
@@ -179,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a)
   // ---- set-up --------------------------------------------------------------------------------
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 128);
+      mbar_init(&full[s], 128 + 4);  // every loader lane's cp.async + one expect-tx per warp
       mbar_init(&empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -352,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a)
       const int64_t t0 = j0 + lw * 32 + lane;
       if (ntiles > 0 && t0 < j1) nxt = __ldg(row + t0);
     }
+    int issued = 0;  // tiles whose copies were issued
     for (int it = 0; it < ntiles; ++it) {
       const int st = it % kStages;
       const int64_t tok0 = j0 + (int64_t)it * kTok;
@@ -376,6 +386,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a)
       }
       const uint32_t kst = sbase + kOffK + st * kTileBytes;
       const uint32_t vst = sbase + kOffV + st * kTileBytes;
+      // when both 16-token halves of this warp's 32 tokens are runs of consecutive slots (whole
+      // pages), they come as TMA boxes, one per 64-element half of K and of V; otherwise all 32
+      // tokens take the 16-byte cp.async path
+      const int64_t s_first = __shfl_sync(0xffffffffu, my, lane & 16);
+      const bool boxes = __all_sync(0xffffffffu, a.use_tma && my >= 0 && my == s_first + (lane & 15));
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes ? 4u * 4096u : 0u);
+      __syncwarp();  // the bytes are expected before any box can land
+      if (boxes) {
+        if ((lane & 15) == 0) {
+          const int t0 = lw * 32 + (lane & 16);  // first token of the run within the tile
+          const int y = a.layer_row0 + (int)my;
+          for (int hf = 0; hf < 2; ++hf) {
+            tc::tma_load_2d(kst + hf * kBlockBytes + t0 * 128, &k16, g * kD + hf * 64, y, &full[st]);
+            tc::tma_load_2d(vst + hf * kBlockBytes + t0 * 128, &v16, g * kD + hf * 64, y, &full[st]);
+          }
+        }
+      } else
 #pragma unroll 4
       for (int j = 0; j < 16; ++j) {
         const int tl = j * 2 + half;          // token within this warp's 32
@@ -388,8 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a)
         tc::cp_async16(vst + off, vg + go, v ? 16u : 0u);
       }
       tc::cp_async_arrive_noinc(&full[st]);
+      issued = it + 1;
     }
     tc::cp_async_wait_all();
+    if (issued < ntiles && lane == 0) {
+      // stopped early: boxes still in flight land before the block can go away
+      for (int u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
+        mbar_wait(&full[u % kStages], (u / kStages) & 1, kDrainLimitNs, a.err);
+    }
   } else {
     // ================================ MMA issuer (one lane) ===================================
     if (lane == 0) {
@@ -450,7 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const DecArgs a)
 }
 
 template <int G>
-cudaError_t run_g(const DecArgs &a, int64_t grid, cudaStream_t s) {
+cudaError_t run_g(const DecArgs &a, const CUtensorMap &k16, const CUtensorMap &v16, int64_t grid,
+                  cudaStream_t s) {
   auto k = decode_tc_kernel<G>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -458,7 +492,7 @@ cudaError_t run_g(const DecArgs &a, int64_t grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a);
+  if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, k16, v16);
   return cudaGetLastError();
 }
 
@@ -497,15 +531,25 @@ cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const vo
   a.max_splits = kv.max_splits;
   a.max_len = kv.max_len;
   a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kv.head_dim));
+  // the pool as a [n_layers * size, Hk * D] tensor for 16-row boxes; TMA row coordinates are
+  // 32-bit, so larger pools take the cp.async path only
+  CUtensorMap k16, v16;
+  memset(&k16, 0, sizeof k16);
+  memset(&v16, 0, sizeof v16);
+  const uint64_t rows = (uint64_t)kv.n_layers * kv.size;
+  const uint64_t cols = (uint64_t)kv.n_kv_heads * kv.head_dim;
+  a.use_tma = rows < (uint64_t(1) << 31) && encode_map_bf16_2d(&k16, kv.k_buffer, rows, cols, 64, 16) &&
+              encode_map_bf16_2d(&v16, kv.v_buffer, rows, cols, 64, 16);
+  a.layer_row0 = a.use_tma ? (int32_t)((int64_t)layer_id * kv.size) : 0;
   const int64_t grid = (int64_t)kv.batch * plan.n_splits * kv.n_kv_heads;
   const int G = n_heads / kv.n_kv_heads;
   cudaError_t e;
   switch (G) {
-    case 1: e = run_g<1>(a, grid, stream); break;
-    case 2: e = run_g<2>(a, grid, stream); break;
-    case 4: e = run_g<4>(a, grid, stream); break;
-    case 8: e = run_g<8>(a, grid, stream); break;
-    case 16: e = run_g<16>(a, grid, stream); break;
+    case 1: e = run_g<1>(a, k16, v16, grid, stream); break;
+    case 2: e = run_g<2>(a, k16, v16, grid, stream); break;
+    case 4: e = run_g<4>(a, k16, v16, grid, stream); break;
+    case 8: e = run_g<8>(a, k16, v16, grid, stream); break;
+    case 16: e = run_g<16>(a, k16, v16, grid, stream); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
