@@ -257,7 +257,7 @@ def run_gpu(args):
     from paged_kv_cache_apply_gb300 import device as DV
     from paged_kv_cache_apply_gb300 import workloads as W
 
-    wl = W.config5()
+    wl = W.mixed_b256_p4x512()
     dw = DV.DeviceWorkload.upload(wl)
     work = step_work(wl)
     chunk, n_splits = A.astr_decode_plan(dw.decode["kv"], wl.n_heads)
@@ -417,7 +417,7 @@ def run_reference(args):
     import numpy as np
     import oracle
     oracle.build()
-    wl = W.config5()
+    wl = W.mixed_b256_p4x512()
     kl = np.ascontiguousarray(wl.pool.k_buffer[0]).copy()
     vl = np.ascontiguousarray(wl.pool.v_buffer[0]).copy()
     dsel, prows = oracle_sample(wl, 1.0 / 16, 1.0 / 16)

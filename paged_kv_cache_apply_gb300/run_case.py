@@ -1,6 +1,6 @@
 """Run one call of the path on one of the synthetic workloads, for timing and profiling.
 
-    python -m paged_kv_cache_apply_gb300.run_case --config 5 --op decode --iters 3 --warmup 1
+    python -m paged_kv_cache_apply_gb300.run_case --workload mixed_b256_p4x512 --op decode --iters 3 --warmup 1
 
 Uploads the seeded workload (see ``workloads``), runs ``--warmup`` untimed calls of the chosen
 op, then ``--iters`` calls timed with CUDA events on the current stream, and prints one JSON
@@ -18,7 +18,9 @@ OPS = ("rope", "prefill", "decode", "step")
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", default="mixed_b256_p4x512",
+                    choices=["tiny_chain", "decode_b64_page1", "prefill_b8_varlen", "long_decode_b4",
+                             "mixed_b256_p4x512"])
     ap.add_argument("--op", default="step", choices=OPS)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=1)
@@ -33,7 +35,7 @@ def main(argv=None):
 
     if not args.no_build:
         B.build()
-    wl = W.make(args.config)
+    wl = W.make(args.workload)
     dw = DV.DeviceWorkload.upload(wl)
     run = {"rope": dw.run_rope, "prefill": dw.run_prefill, "decode": dw.run_decode,
            "step": dw.run_step}[args.op]

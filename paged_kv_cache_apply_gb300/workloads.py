@@ -266,7 +266,7 @@ def _empty_pool(dtype, n_layers, size, hk, d, page_size, num_reqs, max_ctx) -> P
 # ---------------------------------------------------------------------------------------------
 
 
-def config1(seed: int = SEED_BASE + 1) -> Workload:
+def tiny_chain(seed: int = SEED_BASE + 1) -> Workload:
     """Tiny chain, f32: prefill of {7, 13} tokens, then one decode step per request.
 
     1 layer, batch 2, 4 q heads, 2 KV heads, head_dim 64, contiguous pool with
@@ -306,7 +306,7 @@ def config1(seed: int = SEED_BASE + 1) -> Workload:
                     meta={"seed": seed})
 
 
-def config2(seed: int = SEED_BASE + 2, batch: int = 64, lmin: int = 512, lmax: int = 4096,
+def decode_b64_page1(seed: int = SEED_BASE + 2, batch: int = 64, lmin: int = 512, lmax: int = 4096,
             pool_slots: int = 400_000) -> Workload:
     """Decode, bf16, H=16, Hk=4, D=128, page_size 1 over a 400k-slot pool."""
     H, Hk, D = 16, 4, 128
@@ -328,7 +328,7 @@ def config2(seed: int = SEED_BASE + 2, batch: int = 64, lmin: int = 512, lmax: i
                     decode=dec, meta={"seed": seed})
 
 
-def config3(seed: int = SEED_BASE + 3, batch: int = 8, qmin: int = 256, qmax: int = 2048,
+def prefill_b8_varlen(seed: int = SEED_BASE + 3, batch: int = 8, qmin: int = 256, qmax: int = 2048,
             pmax: int = 1024, page: int = 16) -> Workload:
     """Varlen causal prefill, bf16, half the requests resumed after a page-aligned prefix."""
     H, Hk, D = 16, 4, 128
@@ -358,7 +358,7 @@ def config3(seed: int = SEED_BASE + 3, batch: int = 8, qmin: int = 256, qmax: in
                     H, pool, prefill=pre, meta={"seed": seed, "prefix": prefix.tolist()})
 
 
-def config4(seed: int = SEED_BASE + 4, batch: int = 4, lmin: int = 32768, lmax: int = 131072,
+def long_decode_b4(seed: int = SEED_BASE + 4, batch: int = 4, lmin: int = 32768, lmax: int = 131072,
             pool_pages: int = 65536, page: int = 16, chunk: int = 4096) -> Workload:
     """Long-context split-K decode, fixed 4096-token chunks, page_size 16."""
     H, Hk, D = 16, 4, 128
@@ -383,7 +383,7 @@ def config4(seed: int = SEED_BASE + 4, batch: int = 4, lmin: int = 32768, lmax: 
                     pool, decode=dec, meta={"seed": seed})
 
 
-def config5(seed: int = SEED_BASE + 5, n_decode: int = 256, lmin: int = 128, lmax: int = 8192,
+def mixed_b256_p4x512(seed: int = SEED_BASE + 5, n_decode: int = 256, lmin: int = 128, lmax: int = 8192,
             n_prefill: int = 4, chunk_len: int = 512, page: int = 16,
             freqs_max_len: int = 8192) -> Workload:
     """Mixed continuous batch: 256 decode requests + 4 prefill chunks of 512 new tokens.
@@ -433,11 +433,13 @@ def config5(seed: int = SEED_BASE + 5, n_decode: int = 256, lmin: int = 128, lma
                     meta={"seed": seed})
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+WORKLOADS = {f.__name__: f for f in (tiny_chain, decode_b64_page1, prefill_b8_varlen,
+                                    long_decode_b4, mixed_b256_p4x512)}
 
 
-def make(config: int, **kw) -> Workload:
-    return CONFIGS[config](**kw)
+def make(name: str, **kw) -> Workload:
+    """The named workload (a key of WORKLOADS)."""
+    return WORKLOADS[name](**kw)
 
 
 def make_case(dtype: str, n_heads: int, n_kv_heads: int, head_dim: int, page: int, kv_lens,

@@ -31,8 +31,8 @@ def wid(a):
     return W.f32_from_bf16_bits(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
 
 
-def test_config2_decode_page1():
-    wl = W.config2()
+def test_decode_b64_page1():
+    wl = W.decode_b64_page1()
     dw = DV.DeviceWorkload.upload(wl)
     dw.run_decode()
     _sync()
@@ -43,8 +43,8 @@ def test_config2_decode_page1():
     assert err <= TOL_BF16, err
 
 
-def test_config3_varlen_resumed_prefill():
-    wl = W.config3()
+def test_prefill_b8_varlen_resumed():
+    wl = W.prefill_b8_varlen()
     dw = DV.DeviceWorkload.upload(wl)
     dw.run_prefill()
     _sync()
@@ -65,8 +65,8 @@ def test_config3_varlen_resumed_prefill():
     assert err <= TOL_BF16, err
 
 
-def test_config4_long_context_split_decode():
-    wl = W.config4()
+def test_long_decode_b4_split():
+    wl = W.long_decode_b4()
     dw = DV.DeviceWorkload.upload(wl)
     dw.run_decode()
     _sync()
@@ -88,9 +88,9 @@ def test_config4_long_context_split_decode():
     assert np.max(np.abs(lse - (m_p[0, :, :n] + np.log(l_p[0, :, :n])))) <= 1e-3
 
 
-def test_config5_mixed_step():
+def test_mixed_b256_p4x512_step():
     import torch
-    wl = W.config5()
+    wl = W.mixed_b256_p4x512()
     dw = DV.DeviceWorkload.upload(wl)
     k_before = dw.k_buffer.clone()
     dw.run_step()

@@ -69,7 +69,7 @@ def check_cache_equal(dw, layer, kl, vl):
 
 
 def test_tiny_chain():
-    wl = W.config1()
+    wl = W.tiny_chain()
     dw = DV.DeviceWorkload.upload(wl)
     kl, vl = host_layer(wl, 0)
     dw.run_rope()

@@ -421,7 +421,7 @@ def test_resumed_prefill_equals_suffix_of_full_prefill():
 
 def test_tiny_chain_decode_equals_prefill_row():
     # the tiny configuration: prefill {7, 13}, then a decode step at positions 7 and 13
-    wl = W.config1()
+    wl = W.tiny_chain()
     pool = wl.pool
     kl, vl = pool.k_buffer[0], pool.v_buffer[0]
     r = wl.rope

@@ -22,7 +22,7 @@ def test_bf16_rounding_ties_to_even():
 
 
 def test_tiny_config_tables():
-    wl = W.config1()
+    wl = W.tiny_chain()
     assert list(wl.rope.out_cache_loc[:7]) == list(range(7))
     assert list(wl.rope.out_cache_loc[7:]) == list(range(64, 77))
     assert list(wl.rope2.out_cache_loc) == [7, 77]
@@ -47,7 +47,7 @@ def _check_paged(pool, rpi, lens, page):
 
 
 def test_decode_config_small():
-    wl = W.config2(batch=6, lmin=5, lmax=40, pool_slots=500)
+    wl = W.decode_b64_page1(batch=6, lmin=5, lmax=40, pool_slots=500)
     d = wl.decode
     assert np.array_equal(d.kv_indptr, W.prefix_sum(d.seq_lens))
     assert d.max_len == d.seq_lens.max()
@@ -56,7 +56,7 @@ def test_decode_config_small():
 
 
 def test_prefill_config_small():
-    wl = W.config3(batch=6, qmin=10, qmax=300, pmax=64)
+    wl = W.prefill_b8_varlen(batch=6, qmin=10, qmax=300, pmax=64)
     p = wl.prefill
     q = np.diff(p.qo_indptr)
     k = np.diff(p.kv_indptr)
@@ -68,14 +68,14 @@ def test_prefill_config_small():
 
 
 def test_long_decode_config_small():
-    wl = W.config4(batch=3, lmin=100, lmax=400, pool_pages=100, chunk=64)
+    wl = W.long_decode_b4(batch=3, lmin=100, lmax=400, pool_pages=100, chunk=64)
     d = wl.decode
     assert d.split_chunk == 64 and d.max_splits == (400 + 63) // 64
     _check_paged(wl.pool, d.req_pool_indices, d.seq_lens, 16)
 
 
 def test_mixed_config_small():
-    wl = W.config5(n_decode=5, lmin=3, lmax=50, n_prefill=2, chunk_len=20, freqs_max_len=64)
+    wl = W.mixed_b256_p4x512(n_decode=5, lmin=3, lmax=50, n_prefill=2, chunk_len=20, freqs_max_len=64)
     r, d, p = wl.rope, wl.decode, wl.prefill
     assert r.n_tokens == 5 + 40
     assert np.array_equal(r.position_ids[:5], d.seq_lens - 1)
@@ -91,7 +91,7 @@ def test_mixed_config_small():
     assert np.any(k[wl.pool.req_to_token[d.req_pool_indices[0], 0]] != 0) or d.seq_lens[0] == 1
 
 
-@pytest.mark.parametrize("cfg", [1])
-def test_freqs_table_shape(cfg):
-    wl = W.make(cfg)
+@pytest.mark.parametrize("name", ["tiny_chain"])
+def test_freqs_table_shape(name):
+    wl = W.make(name)
     assert wl.rope.freqs_cis.shape == (64, 32, 2)
