@@ -89,18 +89,21 @@ struct Chunk<bf16_t> {
   }
 };
 
-template <typename T>
+// Idx is the integer type of the chunk index: 32-bit whenever the launch's chunks fit, since a
+// 64-bit division is emulated in many instructions and the kernel is otherwise a few loads
+template <typename T, typename Idx>
 __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
-  const int chunks_per_row = a.D >> 3;
+  const int chunk_shift = a.D == 128 ? 4 : 3;  // log2 of the 8-element chunks per row
   const int rows = a.H + 2 * a.Hk;
-  const int64_t per_token = (int64_t)rows * chunks_per_row;
-  const int64_t total = a.n_tokens * per_token;
-  for (int64_t id = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; id < total;
-       id += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = id / per_token;
-    const int c = (int)(id - t * per_token);
-    const int row = c / chunks_per_row;
-    const int e0 = (c - row * chunks_per_row) << 3;
+  const Idx per_token = (Idx)rows << chunk_shift;
+  const Idx total = (Idx)a.n_tokens * per_token;
+  for (Idx id = (Idx)blockIdx.x * blockDim.x + threadIdx.x; id < total;
+       id += (Idx)gridDim.x * blockDim.x) {
+    const Idx tq = id / per_token;
+    const int c = (int)(id - tq * per_token);
+    const int64_t t = (int64_t)tq;  // element offsets below can exceed 32 bits
+    const int row = c >> chunk_shift;
+    const int e0 = (c - (row << chunk_shift)) << 3;
     const int32_t p = __ldg(a.pos + t);
     const int32_t s = __ldg(a.loc + t);
     const bool pos_ok = p >= 0 && p < a.freqs_max_len;
@@ -168,10 +171,15 @@ cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, cons
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms * 32;
   if (blocks > cap) blocks = cap;
-  if (kv.dtype == ASTR_BF16)
-    rope_kv_write_kernel<bf16_t><<<(unsigned)blocks, 256, 0, stream>>>(a);
-  else
-    rope_kv_write_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(a);
+  // the loop's last index reaches total + grid threads, which must not wrap around either
+  const bool narrow = total + blocks * 256 < (int64_t(1) << 32);
+  if (kv.dtype == ASTR_BF16) {
+    if (narrow) rope_kv_write_kernel<bf16_t, uint32_t><<<(unsigned)blocks, 256, 0, stream>>>(a);
+    else rope_kv_write_kernel<bf16_t, int64_t><<<(unsigned)blocks, 256, 0, stream>>>(a);
+  } else {
+    if (narrow) rope_kv_write_kernel<float, uint32_t><<<(unsigned)blocks, 256, 0, stream>>>(a);
+    else rope_kv_write_kernel<float, int64_t><<<(unsigned)blocks, 256, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
