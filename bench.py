@@ -19,6 +19,7 @@ sample of the same step and prints the same line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -96,7 +97,7 @@ def read_peaks():
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -104,6 +105,10 @@ class ClockSampler:
         self.idx = device_index
         self.proc = None
         self.path = None
+        self.window = None  # host wall-clock bounds of the timed region
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def start(self):
         try:
@@ -112,7 +117,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -127,25 +132,31 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]),
+                                 [n for n, v in zip(names, parts[6:10]) if v.lower().startswith("active")]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        # only samples taken inside the timed region count; with none there (a region shorter
+        # than the sampling interval), the nearest ones do and the record says so
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        use = inside if inside else rows
+        sm = [r[1] for r in use]
+        smax = [r[2] for r in use]
+        reasons = set(n for r in use for n in r[3])
+        extra = {"samples": len(use), "in_timed_region": bool(inside)}
+        return dict({"sm_mhz": statistics.median(sm) if sm else None,
+                     "sm_max_mhz": max(smax) if smax else None,
+                     "reasons": sorted(reasons)}, **extra)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -276,6 +287,7 @@ def run_gpu(args):
     time.sleep(0.4)
     barrier(world)
     torch.cuda.synchronize()
+    wall0 = time.time()
     t_start.record(stream)
     for i in range(K):
         ev[i][0].record(stream)
@@ -287,6 +299,7 @@ def run_gpu(args):
         ev[i][3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(wall0, time.time())
     barrier(world)
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
@@ -447,7 +460,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2500)  # about a second of timed work
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
