@@ -127,6 +127,57 @@ class DeviceWorkload:
             d["c"] = d["kv"].as_c()
         return d["c"]
 
+    def step_inputs(self):
+        """What a step takes from the host: the new tokens' q, k, v, positions and slots, and the
+        batch metadata. The cache and the page table stay resident."""
+        out = []
+        if self.rope is not None:
+            r = self.rope
+            out += [r["q"], r["k"], r["v"], r["pos"], r["loc"]]
+        if self.prefill is not None:
+            kv = self.prefill["kv"]
+            out += [kv.req_pool_indices, kv.qo_indptr, kv.kv_indptr, kv.q_tile_to_batch,
+                    kv.q_tile_to_index]
+        if self.decode is not None:
+            kv = self.decode["kv"]
+            out += [kv.req_pool_indices, kv.seq_lens, kv.kv_indptr]
+        return out
+
+    def step_outputs(self):
+        """What a step hands back: the prefill and decode attention outputs."""
+        return [d["out"] for d in (self.prefill, self.decode) if d is not None]
+
+    def pack(self, tensors, align: int = 256):
+        """Moves `tensors` into one contiguous device buffer (each slot `align`-byte aligned) and
+        points every reference of the workload at the new copies, so that one copy moves them
+        all between host and device. Returns the uint8 buffer."""
+        import torch
+        sizes = [t.numel() * t.element_size() for t in tensors]
+        offs, at = [], 0
+        for n in sizes:
+            offs.append(at)
+            at += (n + align - 1) // align * align
+        arena = torch.zeros(at, dtype=torch.uint8, device=tensors[0].device)  # padding stays 0
+        for t, o, n in zip(tensors, offs, sizes):
+            view = arena[o:o + n].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            self._rebind(t, view)
+        self.refresh()
+        return arena
+
+    def _rebind(self, old, new):
+        for d in [self.rope, self.rope2, self.prefill, self.decode, self.decode2]:
+            if d is None:
+                continue
+            for k, v in list(d.items()):
+                if v is old:
+                    d[k] = new
+            kv = d.get("kv")
+            if kv is not None:
+                for name, v in list(vars(kv).items()):
+                    if v is old:
+                        setattr(kv, name, new)
+
     def refresh(self):
         for d in [self.rope, self.rope2, self.prefill, self.decode, self.decode2]:
             if d is not None:
