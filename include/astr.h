@@ -192,6 +192,10 @@ astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *
  * to Q_b; together the tiles must cover every row exactly once. Rows are written only by
  * their tile. bf16 runs on the tcgen05 tensor cores (bf16 operands, f32 accumulation);
  * f32 runs on the CUDA cores in f32 (no TF32).
+ * Tile order changes no result. The bf16 kernel starts its blocks from the END of the tile
+ * list, so listing tiles in request order runs each request's longest (last) tiles first, and
+ * listing them by the number of 128-key tiles they visit, cheapest first, schedules the
+ * costliest first across the whole batch.
  */
 astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
                                    void *out, int32_t n_heads, astr_stream stream);

@@ -155,14 +155,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_saddr, const void *map,
       : "memory");
 }
 
-// warms L2 with the 2-D box at (x, y) of `map`; no shared memory or barrier involved
-__device__ __forceinline__ void tma_prefetch_2d(const void *map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // ---- Ampere-style async copies (16 bytes, zero-filled when src_bytes = 0) -----------------
 __device__ __forceinline__ void cp_async16(uint32_t dst_saddr, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_saddr), "l"(src),
