@@ -121,15 +121,15 @@ int decode_chunk(const astr_kv_cache *kv, int n_heads) {
   if (!kv->decode_o_part || !kv->decode_ml_part || kv->max_splits <= 1) return max_len;
   const bool tc = use_tc_decode(kv, n_heads);
   const int tile = tc ? tc_decode_tile_tokens() : simt_tile_tokens(n_heads / kv->n_kv_heads);
-  // Taking the mean length as half of max_len, aim for about three waves of one resident
-  // block per SM (tensor-core kernel: measured on GB300, longer chunks pay less per-block
-  // start-up and merge work than they lose to the last wave) or four waves of three
-  // (CUDA-core kernel); keep the chunk within [lo, 4096] tokens and never need more splits
-  // than the scratch holds.
+  // Taking the mean length as half of max_len, aim for about nine work items per SM for the
+  // persistent tensor-core kernel (measured on GB300: enough to balance the SMs, few enough
+  // to keep the split-K merge small) or four waves of three resident blocks per SM for the
+  // CUDA-core kernel; keep the chunk within [lo, 4096] tokens and never need more splits than
+  // the scratch holds.
   const int64_t est_tokens = (int64_t)kv->batch * max_len / 2;
-  const int64_t target_blocks = (int64_t)num_sms() * (tc ? 3 : 12);
+  const int64_t target_blocks = (int64_t)num_sms() * (tc ? 9 : 12);
   int64_t c = est_tokens * kv->n_kv_heads / (target_blocks > 0 ? target_blocks : 1);
-  const int64_t lo = tc ? 512 : 256;
+  const int64_t lo = tc ? 1024 : 256;
   if (c < lo) c = lo;
   if (c > 4096) c = 4096;
   const int64_t min_c = (max_len + kv->max_splits - 1) / kv->max_splits;

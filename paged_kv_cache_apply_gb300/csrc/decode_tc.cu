@@ -5,27 +5,38 @@
 // System" (decode_o_part / decode_ml_part split-K partials, merged by log-sum-exp).
 //
 // Decode reads 512 bytes of K+V per token and KV head and does 4*G multiply-adds per byte,
-// so the block is built around the copy pipeline and keeps the arithmetic off the CUDA
-// cores. One block handles (request, chunk, KV head g) with the G query heads of the group:
-//  * warps 4-7 stream 128-token tiles of this head's K and V slices into a 3-stage ring in the
-//    128-byte-swizzled operand layout, 32 tokens per warp: when those are two whole pages (two
-//    runs of 16 consecutive slots) they come as four TMA boxes of 16 rows (one per 64-element
-//    half of K and of V), otherwise as 16-byte cp.async copies (two lane-halves per token row,
-//    fully coalesced) with positions past the chunk zero-filled. Which path a warp takes is
-//    uniform across it, so the copy loop stays the same straight-line code;
-//  * warp 8 allocates 64 TMEM columns and issues, per tile, S^T = K Q^T (M = 128 tokens on
-//    the TMEM lanes, N = 16 query rows of which G are the group, K = 128) into one of two
-//    S buffers, and O^T += V^T P^T (M = 128 = head_dim, N = 16, K = 128 tokens) with V read
-//    as an MN-major operand and P^T from shared memory;
+// so the kernel is built around the copy pipeline and keeps the arithmetic off the CUDA
+// cores. A work item is (request, chunk, KV head g) with the G query heads of the group. The
+// kernel is persistent: one block per SM claims items from a counter until none are left, and
+// its copy pipeline streams from one item into the next without draining, so a block's
+// start-up (3.5 us before its first tile) is paid once per SM instead of once per item:
+//  * warp 9 claims items (split-major: every request's first chunk before any second one, so
+//    the long chunks go first), publishes each through a two-slot ring in shared memory, and
+//    stages the item's query rows in one of two Q buffers;
+//  * warps 4-7 stream 128-token tiles of the item's KV-head slices of K and V into a 3-stage
+//    ring in the 128-byte-swizzled operand layout, 32 tokens per warp: when those are two
+//    whole pages (two runs of 16 consecutive slots) they come as four TMA boxes of 16 rows
+//    (one per 64-element half of K and of V), otherwise as 16-byte cp.async copies (two
+//    lane-halves per token row, fully coalesced) with positions past the chunk zero-filled.
+//    Which path a warp takes is uniform across it, so the copy loop stays straight-line code;
+//  * warp 8 allocates 64 TMEM columns -- two S buffers and two O^T buffers of 16 columns --
+//    and issues, per tile, S^T = K Q^T (M = 128 tokens on the TMEM lanes, N = 16 query rows
+//    of which G are the group, K = 128) and, one tile behind, O^T += V^T P^T (M = 128 =
+//    head_dim, N = 16, K = 128 tokens) with V read as an MN-major operand and P^T from shared
+//    memory; consecutive items accumulate into alternate O^T buffers;
 //  * warps 0-3 (one TMEM lane each) read a token's G scores, take the tile max per head
 //    across the 128 lanes (warp shuffles + one named barrier), keep the softmax reference
 //    max lazily (raised only when a score exceeds it by 2^8, then O^T is rescaled in TMEM),
-//    write P^T in bf16 and, after the last tile, normalise O^T and store the output or the
-//    chunk's partial and (m, l).
+//    write P^T in bf16 and, after an item's last tile, normalise O^T and store the output or
+//    the chunk's partial and (m, l).
+// Tile and item counters run on across items, and every barrier phase follows them.
 // Every wait is bounded; a bad slot is zero-filled and flagged; on a timeout the block stops,
 // waits for its own copies and MMAs, frees TMEM and returns.
 #include <math.h>
 #include <string.h>
+
+#include <atomic>
+#include <mutex>
 
 #include "astr_internal.cuh"
 #include "launch.h"
@@ -42,18 +53,20 @@ constexpr int kNPad = 16;                 // query rows per MMA (N)
 constexpr int kStages = 3;
 constexpr int kTileBytes = kTok * kD * 2; // 32 KB: K (or V) of one tile
 constexpr int kBlockBytes = kTok * 128;   // 16 KB: one 64-element half of a tile
-constexpr int kThreads = 288;             // 4 softmax + 4 loader + 1 MMA warps
+constexpr int kThreads = 320;             // 4 softmax + 4 loader + MMA + scheduler warps
+constexpr int kSchedSlots = 32;           // work counters, used in turn by successive launches
 constexpr float kLazyRescale = 8.0f;
 
 // shared-memory map (offsets from a 1 KB aligned base)
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffQ = kOffV + kStages * kTileBytes;  // 16 rows x 128 -> 2 blocks of 2 KB
-constexpr int kOffP = kOffQ + 4096;                   // 2 buffers x (16 rows x 128 tokens)
+constexpr int kOffQ = kOffV + kStages * kTileBytes;  // 2 buffers x (16 rows x 128: 2 blocks of 2 KB)
+constexpr int kOffP = kOffQ + 2 * 4096;               // 2 buffers x (16 rows x 128 tokens)
 constexpr int kOffRed = kOffP + 2 * 4096;             // [2][4 warps][16] f32 tile maxima
 constexpr int kOffLsum = kOffRed + 2 * 4 * 16 * 4;    // [4 warps][16] f32
 constexpr int kOffBar = kOffLsum + 4 * 16 * 4;
-constexpr int kOffMisc = kOffBar + 32 * 8;
+constexpr int kOffRing = kOffBar + 32 * 8;            // 2 published work items, 64 bytes each
+constexpr int kOffMisc = kOffRing + 2 * 64;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;      // + alignment slack
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kNPad, false, false);
@@ -78,7 +91,33 @@ struct DecArgs {
   int32_t layer_row0;  // first row of this layer in the [n_layers * size, Hk * D] tensor maps
   int32_t use_tma;     // page runs by TMA (the maps' row coordinates fit in 32 bits)
   float scale_log2;
+  int64_t n_items;     // batch * n_splits * Hk work items
+  unsigned *sched;     // [0]: items claimed past the first one of each block, [1]: blocks done
 };
+
+// One work item, (request b, chunk `split`, KV head g), as the scheduler warp hands it to the
+// other roles (ntiles = 0 ends the sequence).
+struct DecItem {
+  int64_t j0, j1;      // positions [j0, j1) of the request
+  const int32_t *row;  // its page-table row
+  int32_t b, g, split, L, ntiles;
+};
+static_assert(sizeof(DecItem) <= 64, "ring slot");
+
+// mbar_wait for a thread nothing waits on closely: it sleeps between polls instead of
+// taking issue slots from the warps it shares a scheduler with
+__device__ __forceinline__ bool sleepy_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                            uint32_t *err) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      raise_error(err, ASTR_DEVERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(500);
+  }
+  return true;
+}
 
 __device__ __forceinline__ bool bar_any(int id, int count, bool pred) {
   uint32_t r;
@@ -150,11 +189,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *full = bars;                 // [kStages] loaders -> MMA (128 + 4 arrivals, TMA bytes)
   uint64_t *empty = bars + kStages;      // [kStages] MMA -> loaders (commit)
-  uint64_t *s_full = bars + 2 * kStages; // [2] MMA -> softmax (commit)
-  uint64_t *p_full = s_full + 2;         // [2] softmax -> MMA (128 arrivals)
-  uint64_t *pv_done = p_full + 2;        // [2] MMA -> softmax (commit)
-  uint64_t *q_full = pv_done + 2;        // softmax -> MMA (128 arrivals)
-  uint64_t *drain = q_full + 1;          // MMA -> itself (commit)
+  uint64_t *s_full = bars + 2 * kStages; // [2] MMA -> softmax (commit), per tile
+  uint64_t *p_full = s_full + 2;         // [2] softmax -> MMA (128 arrivals), per tile
+  uint64_t *pv_done = p_full + 2;        // [2] MMA -> softmax (commit), per tile
+  uint64_t *q_full = pv_done + 2;        // [2] scheduler -> MMA, per item
+  uint64_t *q_empty = q_full + 2;        // [2] MMA commit after an item's last S, per item
+  uint64_t *o_free = q_empty + 2;        // [2] softmax (128 arrivals) read O, per item
+  uint64_t *item_full = o_free + 2;      // [2] scheduler published an item
+  uint64_t *item_empty = item_full + 2;  // [2] loaders (4), MMA (1), softmax (128) took it
+  uint64_t *drain = item_empty + 2;      // MMA -> itself (commit)
+  DecItem *ring = reinterpret_cast<DecItem *>(smem + kOffRing);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
   float *red = reinterpret_cast<float *>(smem + kOffRed);
@@ -163,27 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-
-  // ---- the work item: (request b, chunk `split`, KV head g) ---------------------------------
-  const int g = blockIdx.x % a.Hk;
-  const int64_t wi = blockIdx.x / a.Hk;
-  const int split = (int)(wi % a.n_splits);
-  const int b = (int)(wi / a.n_splits);
-  const int L = __ldg(a.seq_lens + b);
-  if (L < 1 || L > a.max_len || L > a.max_ctx) {
-    if (split == 0 && g == 0 && tid == 0) raise_error(a.err, ASTR_DEVERR_LEN);
-    return;
-  }
-  const int64_t j0 = (int64_t)split * a.chunk;
-  if (j0 >= L) return;
-  const int64_t j1 = j0 + a.chunk < L ? j0 + a.chunk : L;
-  const int r = __ldg(a.rpi + b);
-  if (r < 0 || r >= a.num_reqs) {
-    if (g == 0 && tid == 0) raise_error(a.err, ASTR_DEVERR_ROW);
-    return;
-  }
-  const int32_t *row = a.r2t + (int64_t)r * a.max_ctx;
-  const int ntiles = (int)((j1 - j0 + kTok - 1) / kTok);
 
   // ---- set-up --------------------------------------------------------------------------------
   if (tid == 0) {
@@ -195,8 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&o_free[i], 128);
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], 4 + 1 + 128);
     }
-    mbar_init(q_full, 128);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -205,271 +232,399 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(tmem_slot, 64);
     tc::tmem_relinquish();
   }
-  if (warp < 4) {  // zero Q and both P buffers (rows past the group stay zero)
+  if (warp < 4) {  // zero both Q and both P buffers (rows past the group stay zero)
     uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
-    for (int i = tid; i < (4096 + 8192) / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < (8192 + 8192) / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS0 = tmem, tO = tmem + 32;
+  const uint32_t tS0 = tmem, tO0 = tmem + 32;  // S: 2 x 16 columns; O^T: 2 x 16 columns
+
+  // publication n of the ring: every reader waits, copies and arrives once
+  auto take = [&](uint32_t n, DecItem &w) -> bool {
+    if (!mbar_wait(&item_full[n & 1], (n >> 1) & 1, a.wait_ns, a.err)) return false;
+    w = ring[n & 1];
+    mbar_arrive(&item_empty[n & 1]);
+    return true;
+  };
 
   if (warp < 4) {
     // ============================ softmax / epilogue ===========================================
-    {  // the group's query rows into the Q operand (K-major, swizzled)
-      const uint16_t *qh = static_cast<const uint16_t *>(a.q) + ((int64_t)b * a.H + g * G) * kD;
-      for (int k = tid; k < G * 16; k += 128) {
-        const int h = k >> 4, c = k & 15;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(qh + h * kD) + c);
-        *reinterpret_cast<uint4 *>(smem + kOffQ + tc::sw128_chunk_offset(h, c, 2048)) = v;
-      }
-      tc::fence_proxy_async_smem();
-      mbar_arrive(q_full);
-    }
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m[G], l[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-    }
+    uint32_t it = 0;  // tiles passed, over all items
     bool aborted = false;
-    for (int it = 0; it < ntiles; ++it) {
-      const int sb = it & 1;
-      const int64_t tok0 = j0 + (int64_t)it * kTok;
-      const int n = (int)((j1 - tok0) < kTok ? (j1 - tok0) : kTok);
-      bool ok = true;
-      if (it >= 2) ok = mbar_wait(&pv_done[sb], ((it - 2) >> 1) & 1, a.wait_ns, a.err);
-      ok = ok && mbar_wait(&s_full[sb], (it >> 1) & 1, a.wait_ns, a.err);
-      float x[G];
+    for (uint32_t n = 0; !aborted; ++n) {
+      DecItem w;
+      if (!take(n, w)) {
+        aborted = true;
+        break;
+      }
+      if (w.ntiles == 0) break;
+      const uint32_t tO = tO0 + (n & 1) * 16;
+      float m[G], l[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h) x[h] = -INFINITY;
-      if (ok) {
-        tc::fence_after_sync();
-        float s[G];
-        ld_cols<G>(tS0 + lane_base + sb * 16, s);
-        const bool valid = tid < n;
+      for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+      }
+      for (int j = 0; j < w.ntiles; ++j, ++it) {
+        const int sb = it & 1;
+        const int64_t tok0 = w.j0 + (int64_t)j * kTok;
+        const int nv = (int)((w.j1 - tok0) < kTok ? (w.j1 - tok0) : kTok);
+        bool ok = true;
+        if (it >= 2) ok = mbar_wait(&pv_done[sb], ((it - 2) >> 1) & 1, a.wait_ns, a.err);
+        ok = ok && mbar_wait(&s_full[sb], (it >> 1) & 1, a.wait_ns, a.err);
+        float x[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) x[h] = -INFINITY;
+        if (ok) {
+          tc::fence_after_sync();
+          float s[G];
+          ld_cols<G>(tS0 + lane_base + sb * 16, s);
+          const bool valid = tid < nv;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            x[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
+            float wmax = x[h];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+            if (lane == 0) red[(sb * 4 + warp) * 16 + h] = wmax;
+          }
+        }
+        if (bar_any(1, 128, !ok)) {
+          aborted = true;
+          break;
+        }
+        float mnew[G];
+        bool changed = false;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          x[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
-          float wmax = x[h];
+          float M = red[(sb * 4 + 0) * 16 + h];
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-          if (lane == 0) red[(sb * 4 + warp) * 16 + h] = wmax;
+          for (int q = 1; q < 4; ++q) M = fmaxf(M, red[(sb * 4 + q) * 16 + h]);
+          mnew[h] = (M > m[h] + kLazyRescale) ? M : m[h];
+          changed |= mnew[h] != m[h];
         }
+        if (changed) {  // the same decision in every thread
+          float alpha[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            alpha[h] = ex2_approx(m[h] - mnew[h]);  // 0 while m is still -inf
+            l[h] *= alpha[h];
+            m[h] = mnew[h];
+          }
+          if (j > 0) {  // O^T holds this item's earlier tiles: rescale once PV(it-1) has landed
+            const bool ok2 = mbar_wait(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, a.wait_ns, a.err);
+            if (bar_any(1, 128, !ok2)) {
+              aborted = true;
+              break;
+            }
+            tc::fence_after_sync();
+            float o[G];
+            ld_cols<G>(tO + lane_base, o);
+#pragma unroll
+            for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+            st_cols<G>(tO + lane_base, o);
+          }
+        }
+        // P^T for this tile: token `tid` of query row h
+        unsigned char *pb = smem + kOffP + sb * 4096;
+        const int kb = tid >> 6, within = tid & 63;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float p = (tid < nv) ? ex2_approx(x[h] - m[h]) : 0.f;
+          l[h] += p;
+          const uint32_t off = (uint32_t)kb * 2048u + (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u +
+                               ((uint32_t)((within >> 3) ^ (h & 7)) << 4) + (uint32_t)(within & 7) * 2u;
+          *reinterpret_cast<uint16_t *>(pb + off) = f32_to_bf16_rn(p);
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        mbar_arrive(&p_full[sb]);
       }
+      if (aborted) break;
+      // epilogue: the commit after the item's last P.V covers all of its MMAs
+      const uint32_t last = it - 1;
+      const bool ok = mbar_wait(&pv_done[last & 1], (last >> 1) & 1, a.wait_ns, a.err);
       if (bar_any(1, 128, !ok)) {
         aborted = true;
         break;
       }
-      float mnew[G];
-      bool changed = false;
+      tc::fence_after_sync();
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float M = red[(sb * 4 + 0) * 16 + h];
+      for (int h = 0; h < G; ++h) {  // l over the 128 token lanes
+        float v = l[h];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) M = fmaxf(M, red[(sb * 4 + w) * 16 + h]);
-        mnew[h] = (M > m[h] + kLazyRescale) ? M : m[h];
-        changed |= mnew[h] != m[h];
+        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) lsum_s[warp * 16 + h] = v;
       }
-      if (changed) {  // the same decision in every thread
-        float alpha[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          alpha[h] = ex2_approx(m[h] - mnew[h]);  // 0 while m is still -inf
-          l[h] *= alpha[h];
-          m[h] = mnew[h];
-        }
-        if (it > 0) {  // O^T holds earlier tiles: rescale it once PV(it-1) has landed
-          const bool ok2 = mbar_wait(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1, a.wait_ns, a.err);
-          if (bar_any(1, 128, !ok2)) {
-            aborted = true;
-            break;
-          }
-          tc::fence_after_sync();
-          float o[G];
-          ld_cols<G>(tO + lane_base, o);
-#pragma unroll
-          for (int h = 0; h < G; ++h) o[h] *= alpha[h];
-          st_cols<G>(tO + lane_base, o);
-        }
-      }
-      // P^T for this tile: token `tid` of query row h
-      unsigned char *pb = smem + kOffP + sb * 4096;
-      const int kb = tid >> 6, within = tid & 63;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float p = (tid < n) ? ex2_approx(x[h] - m[h]) : 0.f;
-        l[h] += p;
-        const uint32_t off = (uint32_t)kb * 2048u + (uint32_t)(h >> 3) * 1024u + (uint32_t)(h & 7) * 128u +
-                             ((uint32_t)((within >> 3) ^ (h & 7)) << 4) + (uint32_t)(within & 7) * 2u;
-        *reinterpret_cast<uint16_t *>(pb + off) = f32_to_bf16_rn(p);
-      }
-      tc::fence_proxy_async_smem();
+      bar_sync(1, 128);
+      float o[G];
+      ld_cols<G>(tO + lane_base, o);  // lane = head_dim index `tid`
       tc::fence_before_sync();
-      mbar_arrive(&p_full[sb]);
-    }
-
-    if (!aborted && ntiles > 0) {
-      const int last = ntiles - 1;
-      const bool ok = mbar_wait(&pv_done[last & 1], (last >> 1) & 1, a.wait_ns, a.err);
-      if (bar_any(1, 128, !ok)) {
-        aborted = true;
-      } else {
-        tc::fence_after_sync();
-        // l over the 128 token lanes
+      mbar_arrive(&o_free[n & 1]);  // the next item but one may accumulate into these columns
+      const bool single = a.n_splits == 1 || w.L <= a.chunk;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float v = l[h];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == 0) lsum_s[warp * 16 + h] = v;
-        }
-        bar_sync(1, 128);
-        float o[G];
-        ld_cols<G>(tO + lane_base, o);  // lane = head_dim index `tid`
-        const bool single = a.n_splits == 1 || L <= a.chunk;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float Lh = lsum_s[h] + lsum_s[16 + h] + lsum_s[32 + h] + lsum_s[48 + h];
-          const float val = o[h] / Lh;
-          const int head = g * G + h;
-          if (single) {
-            static_cast<uint16_t *>(a.out)[((int64_t)b * a.H + head) * kD + tid] = f32_to_bf16_rn(val);
-          } else {
-            const int64_t pidx = ((int64_t)b * a.H + head) * a.max_splits + split;
-            a.o_part[pidx * kD + tid] = val;
-            if (tid == 0) {
-              a.ml_part[pidx * 2] = m[h] * 0.69314718055994531f;
-              a.ml_part[pidx * 2 + 1] = Lh;
-            }
+      for (int h = 0; h < G; ++h) {
+        const float Lh = lsum_s[h] + lsum_s[16 + h] + lsum_s[32 + h] + lsum_s[48 + h];
+        const float val = o[h] / Lh;
+        const int head = w.g * G + h;
+        if (single) {
+          static_cast<uint16_t *>(a.out)[((int64_t)w.b * a.H + head) * kD + tid] = f32_to_bf16_rn(val);
+        } else {
+          const int64_t pidx = ((int64_t)w.b * a.H + head) * a.max_splits + w.split;
+          a.o_part[pidx * kD + tid] = val;
+          if (tid == 0) {
+            a.ml_part[pidx * 2] = m[h] * 0.69314718055994531f;
+            a.ml_part[pidx * 2 + 1] = Lh;
           }
         }
       }
+      bar_sync(1, 128);  // lsum_s is rewritten by the next item's epilogue
     }
     if (aborted) *abort_flag = 1;
   } else if (warp < 8) {
     // ================================ loaders =================================================
     const int lw = warp - 4;
     const int64_t rowb = (int64_t)a.Hk * kD * 2;  // bytes between consecutive slots
-    const char *kg = static_cast<const char *>(a.k_layer) + (int64_t)g * kD * 2;
-    const char *vg = static_cast<const char *>(a.v_layer) + (int64_t)g * kD * 2;
     const int half = lane >> 4, c = lane & 15;
-    int64_t nxt = -1;
-    {
-      const int64_t t0 = j0 + lw * 32 + lane;
-      if (ntiles > 0 && t0 < j1) nxt = __ldg(row + t0);
-    }
-    int issued = 0;  // tiles whose copies were issued
-    for (int it = 0; it < ntiles; ++it) {
-      const int st = it % kStages;
-      const int64_t tok0 = j0 + (int64_t)it * kTok;
-      int64_t my = nxt;  // slot of token tok0 + lw*32 + lane (or -1 past the chunk)
-      {
-        const int64_t tn = tok0 + kTok + lw * 32 + lane;
-        nxt = (it + 1 < ntiles && tn < j1) ? (int64_t)__ldg(row + tn) : -1;
-      }
-      if (my >= a.size || (my < 0 && tok0 + lw * 32 + lane < j1)) {
-        raise_error(a.err, ASTR_DEVERR_SLOT);
-        my = -1;
-      }
-      int ok = 1;
-      if (lane == 0) {
-        if (it >= kStages) ok = mbar_wait(&empty[st], ((it / kStages) - 1) & 1, a.wait_ns, a.err);
-        if (*abort_flag) ok = 0;
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        *abort_flag = 1;
+    uint32_t it = 0;      // tiles issued, over all items
+    bool stop = false;
+    for (uint32_t n = 0; !stop; ++n) {
+      // every lane reads the slot; lane 0 releases it once the whole warp has
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&item_full[n & 1], (n >> 1) & 1, a.wait_ns, a.err) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, got, 0)) {
+        stop = true;
         break;
       }
-      const uint32_t kst = sbase + kOffK + st * kTileBytes;
-      const uint32_t vst = sbase + kOffV + st * kTileBytes;
-      // when both 16-token halves of this warp's 32 tokens are runs of consecutive slots (whole
-      // pages), they come as TMA boxes, one per 64-element half of K and of V; otherwise all 32
-      // tokens take the 16-byte cp.async path
-      const int64_t s_first = __shfl_sync(0xffffffffu, my, lane & 16);
-      const bool boxes = __all_sync(0xffffffffu, a.use_tma && my >= 0 && my == s_first + (lane & 15));
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes ? 4u * 4096u : 0u);
-      __syncwarp();  // the bytes are expected before any box can land
-      if (boxes) {
-        if ((lane & 15) == 0) {
-          const int t0 = lw * 32 + (lane & 16);  // first token of the run within the tile
-          const int y = a.layer_row0 + (int)my;
-          for (int hf = 0; hf < 2; ++hf) {
-            tc::tma_load_2d(kst + hf * kBlockBytes + t0 * 128, &k16, g * kD + hf * 64, y, &full[st]);
-            tc::tma_load_2d(vst + hf * kBlockBytes + t0 * 128, &v16, g * kD + hf * 64, y, &full[st]);
-          }
-        }
-      } else
-#pragma unroll 4
-      for (int j = 0; j < 16; ++j) {
-        const int tl = j * 2 + half;          // token within this warp's 32
-        const int t = lw * 32 + tl;           // token within the tile
-        const int64_t s = __shfl_sync(0xffffffffu, my, tl);
-        const uint32_t off = tc::sw128_chunk_offset(t, c, kBlockBytes);
-        const bool v = s >= 0;
-        const int64_t go = v ? s * rowb + c * 16 : 0;
-        tc::cp_async16(kst + off, kg + go, v ? 16u : 0u);
-        tc::cp_async16(vst + off, vg + go, v ? 16u : 0u);
+      mbar_wait(&item_full[n & 1], (n >> 1) & 1, a.wait_ns, a.err);  // completed: acquires at once
+      const DecItem w = ring[n & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[n & 1]);
+      if (w.ntiles == 0) break;
+      const char *kg = static_cast<const char *>(a.k_layer) + (int64_t)w.g * kD * 2;
+      const char *vg = static_cast<const char *>(a.v_layer) + (int64_t)w.g * kD * 2;
+      int64_t nxt = -1;
+      {
+        const int64_t t0 = w.j0 + lw * 32 + lane;
+        if (t0 < w.j1) nxt = __ldg(w.row + t0);
       }
-      tc::cp_async_arrive_noinc(&full[st]);
-      issued = it + 1;
+      for (int j = 0; j < w.ntiles; ++j, ++it) {
+        const int st = it % kStages;
+        const int64_t tok0 = w.j0 + (int64_t)j * kTok;
+        int64_t my = nxt;  // slot of token tok0 + lw*32 + lane (or -1 past the chunk)
+        {
+          const int64_t tn = tok0 + kTok + lw * 32 + lane;
+          nxt = (j + 1 < w.ntiles && tn < w.j1) ? (int64_t)__ldg(w.row + tn) : -1;
+        }
+        if (my >= a.size || (my < 0 && tok0 + lw * 32 + lane < w.j1)) {
+          raise_error(a.err, ASTR_DEVERR_SLOT);
+          my = -1;
+        }
+        int ok = 1;
+        if (lane == 0) {
+          if (it >= kStages) ok = mbar_wait(&empty[st], ((it / kStages) - 1) & 1, a.wait_ns, a.err);
+          if (*abort_flag) ok = 0;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          stop = true;
+          break;
+        }
+        const uint32_t kst = sbase + kOffK + st * kTileBytes;
+        const uint32_t vst = sbase + kOffV + st * kTileBytes;
+        // when both 16-token halves of this warp's 32 tokens are runs of consecutive slots (whole
+        // pages), they come as TMA boxes, one per 64-element half of K and of V; otherwise all 32
+        // tokens take the 16-byte cp.async path
+        const int64_t s_first = __shfl_sync(0xffffffffu, my, lane & 16);
+        const bool boxes = __all_sync(0xffffffffu, a.use_tma && my >= 0 && my == s_first + (lane & 15));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes ? 4u * 4096u : 0u);
+        __syncwarp();  // the bytes are expected before any box can land
+        if (boxes) {
+          if ((lane & 15) == 0) {
+            const int t0 = lw * 32 + (lane & 16);  // first token of the run within the tile
+            const int y = a.layer_row0 + (int)my;
+            for (int hf = 0; hf < 2; ++hf) {
+              tc::tma_load_2d(kst + hf * kBlockBytes + t0 * 128, &k16, w.g * kD + hf * 64, y, &full[st]);
+              tc::tma_load_2d(vst + hf * kBlockBytes + t0 * 128, &v16, w.g * kD + hf * 64, y, &full[st]);
+            }
+          }
+        } else
+#pragma unroll 4
+        for (int jj = 0; jj < 16; ++jj) {
+          const int tl = jj * 2 + half;         // token within this warp's 32
+          const int t = lw * 32 + tl;           // token within the tile
+          const int64_t s = __shfl_sync(0xffffffffu, my, tl);
+          const uint32_t off = tc::sw128_chunk_offset(t, c, kBlockBytes);
+          const bool v = s >= 0;
+          const int64_t go = v ? s * rowb + c * 16 : 0;
+          tc::cp_async16(kst + off, kg + go, v ? 16u : 0u);
+          tc::cp_async16(vst + off, vg + go, v ? 16u : 0u);
+        }
+        tc::cp_async_arrive_noinc(&full[st]);
+      }
     }
     tc::cp_async_wait_all();
-    if (issued < ntiles && lane == 0) {
+    if (stop && lane == 0) {
       // stopped early: boxes still in flight land before the block can go away
-      for (int u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
+      for (uint32_t u = it > kStages ? it - kStages : 0; u < it; ++u)
         mbar_wait(&full[u % kStages], (u / kStages) & 1, kDrainLimitNs, a.err);
     }
+  } else if (warp == 9) {
+    // ============ scheduler: claims items, publishes them, stages their query rows ============
+    // Work positions are split-major (every request's first chunk before any second one), so
+    // the long chunks go first. Block c starts at position c; each further position comes from
+    // the counter once the other roles have taken the block's previous item.
+    const int64_t per_split = (int64_t)a.B * a.Hk;
+    auto claim = [&]() -> int64_t {
+      unsigned got = 0;
+      if (lane == 0) got = atomicAdd(&a.sched[0], 1u);
+      return (int64_t)gridDim.x + __shfl_sync(0xffffffffu, got, 0);
+    };
+    uint32_t n = 0;
+    bool ok = true;
+    int64_t pos = blockIdx.x;
+    while (ok) {
+      DecItem w;
+      w.ntiles = 0;
+      while (pos < a.n_items) {
+        w.split = (int)(pos / per_split);
+        const int rest = (int)(pos % per_split);
+        w.b = rest / a.Hk;
+        w.g = rest % a.Hk;
+        w.L = __ldg(a.seq_lens + w.b);
+        bool good = true;
+        if (w.L < 1 || w.L > a.max_len || w.L > a.max_ctx) {
+          if (w.split == 0 && w.g == 0 && lane == 0) raise_error(a.err, ASTR_DEVERR_LEN);
+          good = false;
+        }
+        w.j0 = (int64_t)w.split * a.chunk;
+        if (good && w.j0 >= w.L) good = false;  // this request has no such chunk
+        const int r = good ? __ldg(a.rpi + w.b) : 0;
+        if (good && (r < 0 || r >= a.num_reqs)) {
+          if (w.split == 0 && w.g == 0 && lane == 0) raise_error(a.err, ASTR_DEVERR_ROW);
+          good = false;
+        }
+        if (good) {
+          w.j1 = w.j0 + a.chunk < w.L ? w.j0 + a.chunk : w.L;
+          w.row = a.r2t + (int64_t)r * a.max_ctx;
+          w.ntiles = (int)((w.j1 - w.j0 + kTok - 1) / kTok);
+          break;
+        }
+        pos = claim();
+      }
+      // publish into slot n & 1 once every reader has taken publication n - 2
+      int fine = 1;
+      if (lane == 0) {
+        if (n >= 2) fine = sleepy_wait(&item_empty[n & 1], ((n >> 1) - 1) & 1, a.wait_ns, a.err);
+        if (fine) {
+          ring[n & 1] = w;
+          mbar_arrive(&item_full[n & 1]);
+        }
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, fine, 0) != 0) || w.ntiles == 0) break;
+      // the item's query rows into Q buffer n & 1 once item n - 2's last S has read it
+      int qok = 1;
+      if (lane == 0 && n >= 2) qok = sleepy_wait(&q_empty[n & 1], ((n >> 1) - 1) & 1, a.wait_ns, a.err);
+      if (!(ok = __shfl_sync(0xffffffffu, qok, 0) != 0)) break;
+      {
+        const uint16_t *qh = static_cast<const uint16_t *>(a.q) + ((int64_t)w.b * a.H + w.g * G) * kD;
+        unsigned char *qs = smem + kOffQ + (n & 1) * 4096;
+        for (int k = lane; k < G * 16; k += 32) {
+          const int h = k >> 4, cc = k & 15;
+          const uint4 v = __ldg(reinterpret_cast<const uint4 *>(qh + h * kD) + cc);
+          *reinterpret_cast<uint4 *>(qs + tc::sw128_chunk_offset(h, cc, 2048)) = v;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[n & 1]);
+      }
+      // claim the next item once this one is taken, so a block holds at most one in reserve
+      int taken = 1;
+      if (lane == 0) taken = sleepy_wait(&item_empty[n & 1], (n >> 1) & 1, a.wait_ns, a.err);
+      if (!(ok = __shfl_sync(0xffffffffu, taken, 0) != 0)) break;
+      ++n;
+      pos = claim();
+    }
+    if (!ok) *abort_flag = 1;
   } else {
     // ================================ MMA issuer (one lane) ===================================
     if (lane == 0) {
-    const uint32_t qaddr = sbase + kOffQ;
-    bool ok = mbar_wait(q_full, 0, a.wait_ns, a.err);
-    auto pv = [&](int i) -> bool {
-      const int sb = i & 1, st = i % kStages;
-      if (!mbar_wait(&p_full[sb], (i >> 1) & 1, a.wait_ns, a.err)) return false;
-      tc::fence_after_sync();
-      tc::fence_proxy_async_smem();
-      const uint32_t vaddr = sbase + kOffV + st * kTileBytes;
-      const uint32_t paddr = sbase + kOffP + sb * 4096;
+      // O^T += V^T P^T for tile i (P^T from buffer i & 1) into O buffer ob; `first` starts it
+      auto pv = [&](uint32_t i, int ob, bool first) -> bool {
+        const int sb = i & 1, st = i % kStages;
+        if (!mbar_wait(&p_full[sb], (i >> 1) & 1, a.wait_ns, a.err)) return false;
+        tc::fence_after_sync();
+        tc::fence_proxy_async_smem();
+        const uint32_t vaddr = sbase + kOffV + st * kTileBytes;
+        const uint32_t paddr = sbase + kOffP + sb * 4096;
 #pragma unroll
-      for (int ks = 0; ks < kTok / 16; ++ks) {
-        const uint64_t ad = tc::desc_sw128(vaddr + ks * 2048, kBlockBytes, 1024);
-        const uint64_t bd = tc::desc_sw128(paddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
-        tc::mma_ss(tO, ad, bd, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
-      }
-      tc::mma_commit(&empty[st]);
-      tc::mma_commit(&pv_done[sb]);
-      return true;
-    };
-    if (ok) {
-      tc::fence_after_sync();
-      for (int it = 0; it < ntiles && ok; ++it) {
-        const int st = it % kStages, sb = it & 1;
-        if (*abort_flag || !mbar_wait(&full[st], (it / kStages) & 1, a.wait_ns, a.err)) {
+        for (int ks = 0; ks < kTok / 16; ++ks) {
+          const uint64_t ad = tc::desc_sw128(vaddr + ks * 2048, kBlockBytes, 1024);
+          const uint64_t bd = tc::desc_sw128(paddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
+          tc::mma_ss(tO0 + ob * 16, ad, bd, kIdescPV, (!first || ks > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&empty[st]);
+        tc::mma_commit(&pv_done[sb]);
+        return true;
+      };
+      bool ok = true;
+      uint32_t it = 0;                 // tiles issued, over all items
+      bool have_prev = false;          // a tile whose P.V is still to be issued
+      int prev_ob = 0;
+      bool prev_first = false;
+      for (uint32_t n = 0; ok; ++n) {
+        DecItem w;
+        if (!take(n, w)) {
           ok = false;
           break;
         }
-        tc::fence_after_sync();
-        tc::fence_proxy_async_smem();
-        const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint64_t ad = tc::desc_sw128(kaddr + (ks >> 2) * kBlockBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::desc_sw128(qaddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
-          tc::mma_ss(tS0 + sb * 16, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+        if (w.ntiles == 0) break;
+        const int qb = n & 1, ob = n & 1;
+        if (!mbar_wait(&q_full[qb], (n >> 1) & 1, a.wait_ns, a.err)) {
+          ok = false;
+          break;
         }
-        tc::mma_commit(&s_full[sb]);
-        if (it > 0 && !pv(it - 1)) ok = false;
+        const uint32_t qaddr = sbase + kOffQ + qb * 4096;
+        for (int j = 0; j < w.ntiles && ok; ++j, ++it) {
+          const int st = it % kStages, sb = it & 1;
+          if (*abort_flag || !mbar_wait(&full[st], (it / kStages) & 1, a.wait_ns, a.err)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          tc::fence_proxy_async_smem();
+          const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint64_t ad = tc::desc_sw128(kaddr + (ks >> 2) * kBlockBytes + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = tc::desc_sw128(qaddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
+            tc::mma_ss(tS0 + sb * 16, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&s_full[sb]);
+          if (j + 1 == w.ntiles) tc::mma_commit(&q_empty[qb]);  // the item's last read of Q
+          if (have_prev && !pv(it - 1, prev_ob, prev_first)) {
+            ok = false;
+            break;
+          }
+          // this tile's P.V goes in after the next tile's S; the first one of an item waits for
+          // the epilogue of the item two back to have read the O buffer
+          if (j == 0 && n >= 2 && !mbar_wait(&o_free[ob], ((n >> 1) - 1) & 1, a.wait_ns, a.err)) {
+            ok = false;
+            break;
+          }
+          have_prev = true;
+          prev_ob = ob;
+          prev_first = j == 0;
+        }
       }
-      if (ok && ntiles > 0 && !pv(ntiles - 1)) ok = false;
-    }
-    if (!ok) *abort_flag = 1;
-    tc::mma_commit(drain);  // nothing may still be in flight when TMEM is freed
-    mbar_wait(drain, 0, kDrainLimitNs, a.err);
+      if (ok && have_prev && !pv(it - 1, prev_ob, prev_first)) ok = false;
+      if (!ok) *abort_flag = 1;
+      tc::mma_commit(drain);  // nothing may still be in flight when TMEM is freed
+      mbar_wait(drain, 0, kDrainLimitNs, a.err);
     }
     __syncwarp();
   }
@@ -480,6 +635,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 64);
   }
+  if (tid == 0) {
+    // the last block to finish resets the counters for the next launch that uses them (every
+    // block has made its last claim before its __syncthreads above)
+    __threadfence();
+    if (atomicAdd(&a.sched[1], 1u) == gridDim.x - 1) {
+      atomicExch(&a.sched[0], 0u);
+      atomicExch(&a.sched[1], 0u);
+    }
+  }
+}
+
+// Work counters: each launch takes the next of kSchedSlots pairs, so launches that overlap
+// on different streams use different ones unless kSchedSlots of them run at once. A launch's
+// last block puts its pair back to zero.
+__device__ unsigned g_dec_sched[2 * kSchedSlots];
+constexpr int kMaxDevices = 64;
+std::mutex g_sched_mutex;
+unsigned *g_sched_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::atomic<unsigned> g_sched_next{0};
+
+cudaError_t sched_slot(unsigned **out, int *sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(g_sched_mutex);
+    if (!g_sched_ptr[dev]) {
+      void *p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_dec_sched)) != cudaSuccess) return e;
+      if ((e = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+      g_sched_ptr[dev] = static_cast<unsigned *>(p);
+    }
+  }
+  *out = g_sched_ptr[dev] + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
+  *sms = g_sms[dev];
+  return cudaSuccess;
 }
 
 template <int G>
@@ -541,7 +735,12 @@ cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const vo
   a.use_tma = rows < (uint64_t(1) << 31) && encode_map_bf16_2d(&k16, kv.k_buffer, rows, cols, 64, 16) &&
               encode_map_bf16_2d(&v16, kv.v_buffer, rows, cols, 64, 16);
   a.layer_row0 = a.use_tma ? (int32_t)((int64_t)layer_id * kv.size) : 0;
-  const int64_t grid = (int64_t)kv.batch * plan.n_splits * kv.n_kv_heads;
+  a.n_items = (int64_t)kv.batch * plan.n_splits * kv.n_kv_heads;
+  int sms = 0;
+  cudaError_t se = sched_slot(&a.sched, &sms);
+  if (se != cudaSuccess) return se;
+  // one block per SM: the blocks claim work items until none are left
+  const int64_t grid = a.n_items < sms ? a.n_items : sms;
   const int G = n_heads / kv.n_kv_heads;
   cudaError_t e;
   switch (G) {
