@@ -146,9 +146,7 @@ astr_status astr_rope_kv_write(const astr_kv_cache *kv, int32_t layer_id, const 
  * The bf16 head_dim-128 kernel is persistent: one block per SM takes (request, chunk, KV
  * head) items from a work counter in device memory that belongs to the library. Each call uses
  * the next of 32 such counters on the current device (its last block resets it), so calls
- * overlapping on different streams stay independent unless 32 of them run at once. Replays
- * of one captured CUDA graph reuse the counter chosen at capture time, and a graph never runs
- * concurrently with itself.
+ * overlapping on different streams stay independent unless 32 of them run at once.
  */
 astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
                                   int32_t n_heads, astr_stream stream);
