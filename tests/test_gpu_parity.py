@@ -331,6 +331,29 @@ def test_tiny_wait_limit_never_faults():
     assert maxerr(DV.to_host(dw.decode["out"]), ref) <= TOL["bf16"]
 
 
+def test_concurrent_decodes_on_two_streams():
+    # the persistent decode takes its work items from a per-call counter: calls in flight at the
+    # same time on different streams must not take each other's items
+    import torch
+    cases = []
+    for k, lens in enumerate([[900, 3000, 17, 5000], [4096, 1, 2500, 700, 128]]):
+        wl = W.make_case("bf16", 16, 4, 128, 16, lens, None, split_chunk=0, max_splits=64,
+                         seed=W.SEED_BASE + 700 + k)
+        cases.append((wl, DV.DeviceWorkload.upload(wl)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    _sync()
+    for rep in range(3):
+        for (wl, dw), s in zip(cases, streams):
+            dw.run_decode(stream=s.cuda_stream)
+    _sync()
+    for wl, dw in cases:
+        kl, vl = host_layer(wl, 1)
+        d = wl.decode
+        ref = oracle.decode(d.q, kl, vl, wl.pool.req_to_token, d.req_pool_indices, d.seq_lens)
+        assert maxerr(DV.to_host(dw.decode["out"]), ref) <= TOL["bf16"]
+    assert A.astr_device_error() == 0
+
+
 def test_empty_batches_are_no_ops():
     import torch
     wl = W.make_case("bf16", 8, 2, 64, 16, [20], None)
