@@ -171,6 +171,29 @@ astr_status astr_decode_attention_noalloc(const astr_kv_cache *kv, int32_t layer
                                           const void *q, int32_t n_heads, astr_stream stream);
 
 /*
+ * Decode with RoPE and the new token's cache write folded in, in one launch (plus the split-K
+ * merge): the decode path of the inference guide's "Attention Backend" writes the new token's
+ * K/V while calling the paged decode op; "Rotary Position Embedding (RoPE)" (internals page)
+ * rotates q and k before the cache write.
+ *
+ * For request b: q[b] ([batch, n_heads, head_dim], not rotated yet) is rotated by the
+ * (cos, sin) row freqs_cis[position_ids[b]]; k_new[b] ([batch, n_kv_heads, head_dim]) is
+ * rotated the same way and written, with v_new[b] unchanged, into slot kv->out_cache_loc[b]
+ * of layer `layer_id`; then decode_out[b] is computed exactly as astr_decode_attention does,
+ * with the rotated query. Rounding is that of astr_rope_kv_write, so the cache bytes are the
+ * same as a rotate + write call would leave. out_cache_loc[b] must be the slot of the
+ * request's newest position, req_to_token[req_pool_indices[b], seq_lens[b] - 1]. q is read
+ * only (the rotated query is not written back). A position or slot out of range raises
+ * ASTR_DEVERR_POS / _SLOT in the error word and that token is neither rotated nor written.
+ * Serves bf16 with head_dim 128 (the tensor-core decode) and returns ASTR_ERR_UNSUPPORTED
+ * otherwise. The pages name no such single call: their RoPE runs as a separate step.
+ */
+astr_status astr_decode_attention_rope(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                                       const void *k_new, const void *v_new, int32_t n_heads,
+                                       const float *freqs_cis, int32_t freqs_max_len,
+                                       const int32_t *position_ids, astr_stream stream);
+
+/*
  * The split plan astr_decode_attention would use for `kv`: chunk length and the number of
  * splits ceil(max_len / chunk). Host-only; enqueues nothing.
  */

@@ -66,6 +66,7 @@ def lib():
             L.astr_rope_kv_write.argtypes = [KV, I32, P, P, P, P, I32, P, I32, P, P]
             L.astr_decode_attention.argtypes = [KV, I32, P, I32, P]
             L.astr_decode_attention_noalloc.argtypes = [KV, I32, P, I32, P]
+            L.astr_decode_attention_rope.argtypes = [KV, I32, P, P, P, I32, P, I32, P, P]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
             L.astr_prefill_attention.argtypes = [KV, I32, P, P, I32, P]
             L.astr_last_error.restype = C.c_char_p
@@ -76,7 +77,7 @@ def lib():
             L.astr_version.restype = I32
             L.astr_kv_cache_bytes.restype = I32
             for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
-                         "astr_decode_attention_noalloc",
+                         "astr_decode_attention_noalloc", "astr_decode_attention_rope",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -206,6 +207,16 @@ def astr_decode_attention(kv, layer_id, q, n_heads, stream=None) -> None:
     c = _kv(kv)
     _check(lib().astr_decode_attention(C.byref(c), int(layer_id), _ptr(q), int(n_heads),
                                        _stream(stream)))
+
+
+def astr_decode_attention_rope(kv, layer_id: int, q, k_new, v_new, n_heads: int, freqs_cis,
+                               freqs_max_len: int, position_ids, stream=None) -> None:
+    """Decode with RoPE and the new token's K/V write folded in (q, k_new not rotated yet)."""
+    c = _kv(kv)
+    _check(lib().astr_decode_attention_rope(C.byref(c), int(layer_id), _ptr(q), _ptr(k_new),
+                                            _ptr(v_new), int(n_heads), _ptr(freqs_cis),
+                                            int(freqs_max_len), _ptr(position_ids),
+                                            _stream(stream)))
 
 
 def astr_decode_attention_noalloc(kv, layer_id, q, n_heads, stream=None) -> None:

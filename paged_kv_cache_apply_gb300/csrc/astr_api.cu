@@ -211,6 +211,13 @@ cudaError_t launch_validate(const astr_kv_cache &kv, int what, uint32_t *err, cu
 
 }  // namespace astr
 
+namespace astr {
+namespace {
+astr_status decode_impl(const astr_kv_cache *kv, int32_t layer_id, const void *q, int32_t n_heads,
+                        astr_stream stream, const DecodeRope *rope);
+}  // namespace
+}  // namespace astr
+
 using namespace astr;
 
 extern "C" {
@@ -299,6 +306,41 @@ astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *
 
 astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
                                   int32_t n_heads, astr_stream stream) {
+  return decode_impl(kv, layer_id, q, n_heads, stream, nullptr);
+}
+
+astr_status astr_decode_attention_rope(const astr_kv_cache *kv, int32_t layer_id, const void *q,
+                                       const void *k_new, const void *v_new, int32_t n_heads,
+                                       const float *freqs_cis, int32_t freqs_max_len,
+                                       const int32_t *position_ids, astr_stream stream) {
+  astr_status st = check_cache(kv, layer_id, n_heads);
+  if (st != ASTR_OK) return st;
+  if (!use_tc_decode(kv, n_heads))
+    return fail(ASTR_ERR_UNSUPPORTED,
+                "decode with RoPE folded in serves bf16, head_dim 128 and group sizes 1/2/4/8/16; "
+                "use astr_rope_kv_write + astr_decode_attention");
+  if (kv->batch > 0) {
+    if (!k_new || !v_new || !freqs_cis || !position_ids || !kv->out_cache_loc)
+      return fail(ASTR_ERR_INVALID, "k_new, v_new, freqs_cis, position_ids and out_cache_loc must be non-NULL");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(freqs_cis))
+      return fail(ASTR_ERR_INVALID, "k_new, v_new and freqs_cis must be 16-byte aligned");
+    if (freqs_max_len < 1) return fail(ASTR_ERR_INVALID, "freqs_max_len %d < 1", freqs_max_len);
+  }
+  DecodeRope r;
+  r.k_new = k_new;
+  r.v_new = v_new;
+  r.freqs = freqs_cis;
+  r.freqs_max_len = freqs_max_len;
+  r.position_ids = position_ids;
+  return decode_impl(kv, layer_id, q, n_heads, stream, &r);
+}
+
+}  // extern "C"
+
+namespace astr {
+namespace {
+astr_status decode_impl(const astr_kv_cache *kv, int32_t layer_id, const void *q, int32_t n_heads,
+                        astr_stream stream, const DecodeRope *rope) {
   astr_status st = check_cache(kv, layer_id, n_heads);
   if (st != ASTR_OK) return st;
   if (kv->batch < 0) return fail(ASTR_ERR_INVALID, "batch %d < 0", kv->batch);
@@ -333,12 +375,16 @@ astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, con
   if (g_checked.load() && (e = launch_validate(*kv, VALIDATE_DECODE, plan.err, s)) != cudaSuccess)
     return cuda_fail(e, "checked-mode validation launch");
   if (use_tc_decode(kv, n_heads))
-    e = launch_tc_decode(*kv, layer_id, q, n_heads, plan, s);
+    e = launch_tc_decode(*kv, layer_id, q, n_heads, plan, s, rope);
   else
     e = launch_simt_attention(*kv, layer_id, q, kv->decode_out, n_heads, plan, s);
   if (e != cudaSuccess) return cuda_fail(e, "astr_decode_attention launch");
   return finish(s);
 }
+}  // namespace
+}  // namespace astr
+
+extern "C" {
 
 astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
                                    void *out, int32_t n_heads, astr_stream stream) {

@@ -37,6 +37,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return r;
 }
 
+// RoPE on four adjacent (x[2i], x[2i+1]) pairs with (cos, sin) pairs cs (AstrAI internals,
+// "Rotary Position Embedding (RoPE)"; inference guide, "Rotary Embedding Backend": the complex
+// product of view_as_complex pairs). Every product and sum is rounded separately (no FMA), so
+// the result does not depend on the compiler's contraction choices.
+__device__ __forceinline__ void rotate4(const float (&x)[8], const float (&cs)[8], float (&y)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = x[2 * i], b = x[2 * i + 1], c = cs[2 * i], s = cs[2 * i + 1];
+    y[2 * i] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+    y[2 * i + 1] = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // packed f32x2 arithmetic (sm_100 family)
 // ------------------------------------------------------------------------------------------

@@ -93,6 +93,15 @@ struct DecArgs {
   float scale_log2;
   int64_t n_items;     // batch * n_splits * Hk work items
   unsigned *sched;     // [0]: items claimed past the first one of each block, [1]: blocks done
+  // RoPE and the new token's cache write folded in (astr_decode_attention_rope); fused = 0
+  // for plain decode
+  const void *k_new;   // [B, Hk, D]: the new token's key, rotated here
+  const void *v_new;   // [B, Hk, D]: its value
+  const float *freqs;  // [freqs_max_len, D / 2, 2] (cos, sin)
+  const int32_t *pos;  // [B] position of the new token
+  const int32_t *loc;  // [B] its cache slot
+  int32_t freqs_max_len;
+  int32_t fused;
 };
 
 // One work item, (request b, chunk `split`, KV head g), as the scheduler warp hands it to the
@@ -516,6 +525,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pos = claim();
       }
+      // with RoPE folded in: the query position and, for the chunk that ends at the newest
+      // position, that token's rotated key and its value written into its cache slot before the
+      // item is published, so the loaders' copies of that tile read them
+      bool qrot = false;
+      const float *cs_row = nullptr;
+      if (a.fused && w.ntiles > 0) {
+        const int p = __ldg(a.pos + w.b);
+        const int32_t sl = __ldg(a.loc + w.b);
+        const bool pos_ok = p >= 0 && p < a.freqs_max_len;
+        const bool slot_ok = sl >= 0 && (int64_t)sl < a.size;
+        if (!(pos_ok && slot_ok) && lane == 0)
+          raise_error(a.err, (pos_ok ? 0u : ASTR_DEVERR_POS) | (slot_ok ? 0u : ASTR_DEVERR_SLOT));
+        qrot = pos_ok;
+        cs_row = a.freqs + (int64_t)p * kD;
+        if (pos_ok && slot_ok && w.j1 == w.L && lane < 16) {
+          const int e0 = lane * 8;
+          float cs[8], x[8], y[8];
+          const float4 f0 = __ldg(reinterpret_cast<const float4 *>(cs_row + e0));
+          const float4 f1 = __ldg(reinterpret_cast<const float4 *>(cs_row + e0) + 1);
+          cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+          cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
+          const int64_t src = ((int64_t)w.b * a.Hk + w.g) * kD + e0;
+          const int64_t dst = ((int64_t)sl * a.Hk + w.g) * kD + e0;
+          const uint4 kr = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.k_new) + src));
+          x[0] = bf16_lo(kr.x); x[1] = bf16_hi(kr.x); x[2] = bf16_lo(kr.y); x[3] = bf16_hi(kr.y);
+          x[4] = bf16_lo(kr.z); x[5] = bf16_hi(kr.z); x[6] = bf16_lo(kr.w); x[7] = bf16_hi(kr.w);
+          rotate4(x, cs, y);
+          uint4 ko;
+          ko.x = pack_bf16x2_rn(y[0], y[1]);
+          ko.y = pack_bf16x2_rn(y[2], y[3]);
+          ko.z = pack_bf16x2_rn(y[4], y[5]);
+          ko.w = pack_bf16x2_rn(y[6], y[7]);
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(const_cast<void *>(a.k_layer)) + dst) = ko;
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(const_cast<void *>(a.v_layer)) + dst) =
+              __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.v_new) + src));
+          // the loaders may read the row by TMA (async proxy) or cp.async
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence_block();
+        }
+        __syncwarp();
+      }
       // publish into slot n & 1 once every reader has taken publication n - 2
       int fine = 1;
       if (lane == 0) {
@@ -535,7 +585,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char *qs = smem + kOffQ + (n & 1) * 4096;
         for (int k = lane; k < G * 16; k += 32) {
           const int h = k >> 4, cc = k & 15;
-          const uint4 v = __ldg(reinterpret_cast<const uint4 *>(qh + h * kD) + cc);
+          uint4 v = __ldg(reinterpret_cast<const uint4 *>(qh + h * kD) + cc);
+          if (qrot) {  // RoPE on the query, rounded as the separate rotate + write call does
+            float cs[8], x[8], y[8];
+            const float4 f0 = __ldg(reinterpret_cast<const float4 *>(cs_row + cc * 8));
+            const float4 f1 = __ldg(reinterpret_cast<const float4 *>(cs_row + cc * 8) + 1);
+            cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+            cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
+            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+            rotate4(x, cs, y);
+            v.x = pack_bf16x2_rn(y[0], y[1]);
+            v.y = pack_bf16x2_rn(y[2], y[3]);
+            v.z = pack_bf16x2_rn(y[4], y[5]);
+            v.w = pack_bf16x2_rn(y[6], y[7]);
+          }
           *reinterpret_cast<uint4 *>(qs + tc::sw128_chunk_offset(h, cc, 2048)) = v;
         }
         tc::fence_proxy_async_smem();
@@ -700,8 +764,16 @@ bool tc_decode_supported(int dtype, int head_dim, int group) {
 int tc_decode_tile_tokens() { return kTok; }
 
 cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const void *q,
-                             int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream) {
+                             int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream,
+                             const DecodeRope *rope) {
   DecArgs a;
+  a.fused = rope != nullptr;
+  a.k_new = rope ? rope->k_new : nullptr;
+  a.v_new = rope ? rope->v_new : nullptr;
+  a.freqs = rope ? rope->freqs : nullptr;
+  a.pos = rope ? rope->position_ids : nullptr;
+  a.loc = rope ? kv.out_cache_loc : nullptr;
+  a.freqs_max_len = rope ? rope->freqs_max_len : 0;
   const int64_t layer_elems = (int64_t)layer_id * kv.size * kv.n_kv_heads * kv.head_dim;
   a.q = q;
   a.k_layer = static_cast<const char *>(kv.k_buffer) + layer_elems * 2;

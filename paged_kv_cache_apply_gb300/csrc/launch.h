@@ -37,8 +37,17 @@ cudaError_t launch_split_merge(const astr_kv_cache &kv, int32_t n_heads, const S
 // tcgen05 bf16 decode (head_dim 128)
 bool tc_decode_supported(int dtype, int head_dim, int group);
 int tc_decode_tile_tokens();
+// RoPE and the new token's cache write folded into the decode (astr_decode_attention_rope)
+struct DecodeRope {
+  const void *k_new;
+  const void *v_new;
+  const float *freqs;
+  int32_t freqs_max_len;
+  const int32_t *position_ids;
+};
 cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const void *q,
-                             int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream);
+                             int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream,
+                             const DecodeRope *rope = nullptr);
 
 // tcgen05 bf16 prefill.
 bool tc_prefill_supported(int dtype, int head_dim, int group, int q_tile_rows);

@@ -35,15 +35,6 @@ struct RopeArgs {
   uint32_t *err;
 };
 
-__device__ __forceinline__ void rotate4(const float (&x)[8], const float (&cs)[8], float (&y)[8]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = x[2 * i], b = x[2 * i + 1], c = cs[2 * i], s = cs[2 * i + 1];
-    y[2 * i] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
-    y[2 * i + 1] = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
-  }
-}
-
 template <typename T>
 struct Chunk;
 
