@@ -194,6 +194,27 @@ astr_status astr_decode_attention_rope(const astr_kv_cache *kv, int32_t layer_id
                                        const int32_t *position_ids, astr_stream stream);
 
 /*
+ * The per-step metadata of a prefill batch, on the HOST (inference guide, "KVCache System":
+ * qo_indptr, kv_indptr and the q_tile_to_batch / q_tile_to_index maps, computed once per step
+ * and shared by every layer; internals page, "Attention Backend").
+ *
+ * From q_lens[b] (new rows) and kv_lens[b] (keys, cached prefix included; q_len <= kv_len)
+ * for b < batch, writes qo_indptr[0..batch] and kv_indptr[0..batch] (prefix sums) and one
+ * entry per q_tile_rows-row Q tile to q_tile_to_batch / q_tile_to_index, listed by the number
+ * of 128-key tiles the Q tile visits under the causal mask, cheapest first (ties in request
+ * order): the order in which the bf16 prefill balances best (it starts from the end of the
+ * list). *num_tiles receives the tile count. All pointers are host memory owned by the
+ * caller; the indptrs (batch + 1 entries each) are required even for batch 0, q_lens and
+ * kv_lens may be NULL only when batch is 0, and the maps (room for max_tiles entries) only
+ * when there are no tiles. Returns ASTR_ERR_INVALID for bad lengths
+ * or too small a max_tiles (*num_tiles still holds the count needed). Enqueues nothing.
+ */
+astr_status astr_prefill_tiles(const int32_t *q_lens, const int32_t *kv_lens, int32_t batch,
+                               int32_t q_tile_rows, int32_t *qo_indptr, int32_t *kv_indptr,
+                               int32_t *q_tile_to_batch, int32_t *q_tile_to_index,
+                               int32_t max_tiles, int32_t *num_tiles);
+
+/*
  * The split plan astr_decode_attention would use for `kv`: chunk length and the number of
  * splits ceil(max_len / chunk). Host-only; enqueues nothing.
  */

@@ -67,6 +67,8 @@ def lib():
             L.astr_decode_attention.argtypes = [KV, I32, P, I32, P]
             L.astr_decode_attention_noalloc.argtypes = [KV, I32, P, I32, P]
             L.astr_decode_attention_rope.argtypes = [KV, I32, P, P, P, I32, P, I32, P, P]
+            PI = C.POINTER(I32)
+            L.astr_prefill_tiles.argtypes = [PI, PI, I32, I32, PI, PI, PI, PI, I32, PI]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
             L.astr_prefill_attention.argtypes = [KV, I32, P, P, I32, P]
             L.astr_last_error.restype = C.c_char_p
@@ -78,6 +80,7 @@ def lib():
             L.astr_kv_cache_bytes.restype = I32
             for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
                          "astr_decode_attention_noalloc", "astr_decode_attention_rope",
+                         "astr_prefill_tiles",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -224,6 +227,27 @@ def astr_decode_attention_noalloc(kv, layer_id, q, n_heads, stream=None) -> None
     c = _kv(kv)
     _check(lib().astr_decode_attention_noalloc(C.byref(c), int(layer_id), _ptr(q), int(n_heads),
                                                _stream(stream)))
+
+
+def astr_prefill_tiles(q_lens, kv_lens, q_tile_rows: int = 128):
+    """Host-side prefill metadata: (qo_indptr, kv_indptr, q_tile_to_batch, q_tile_to_index) as
+    int32 numpy arrays, the tiles cheapest first."""
+    import numpy as np
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    kl = np.ascontiguousarray(kv_lens, dtype=np.int32)
+    B = int(ql.size)
+    P = C.POINTER(C.c_int32)
+    ptr = lambda a: a.ctypes.data_as(P)
+    n = C.c_int32(0)
+    qo, kv = np.zeros(B + 1, np.int32), np.zeros(B + 1, np.int32)
+    st = lib().astr_prefill_tiles(ptr(ql), ptr(kl), B, int(q_tile_rows), ptr(qo), ptr(kv), None, None,
+                                  0, C.byref(n))
+    tb, ti = np.zeros(max(n.value, 1), np.int32), np.zeros(max(n.value, 1), np.int32)
+    if st != 0 and n.value == 0:
+        _check(st)
+    _check(lib().astr_prefill_tiles(ptr(ql), ptr(kl), B, int(q_tile_rows), ptr(qo), ptr(kv), ptr(tb),
+                                    ptr(ti), n.value, C.byref(n)))
+    return qo, kv, tb[:n.value], ti[:n.value]
 
 
 def astr_decode_plan(kv, n_heads):

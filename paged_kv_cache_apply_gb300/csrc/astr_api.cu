@@ -5,8 +5,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <string>
+#include <vector>
 
 #include "astr_internal.cuh"
 #include "launch.h"
@@ -301,6 +303,55 @@ astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *
   const int c = decode_chunk(kv, n_heads);
   *split_chunk = c;
   *n_splits = (kv->max_len + c - 1) / c;
+  return ok();
+}
+
+astr_status astr_prefill_tiles(const int32_t *q_lens, const int32_t *kv_lens, int32_t batch,
+                               int32_t q_tile_rows, int32_t *qo_indptr, int32_t *kv_indptr,
+                               int32_t *q_tile_to_batch, int32_t *q_tile_to_index,
+                               int32_t max_tiles, int32_t *num_tiles) {
+  if (!num_tiles || !qo_indptr || !kv_indptr || (batch > 0 && (!q_lens || !kv_lens)))
+    return fail(ASTR_ERR_INVALID, "NULL argument");
+  if (batch < 0 || q_tile_rows < 1 || max_tiles < 0)
+    return fail(ASTR_ERR_INVALID, "batch %d, q_tile_rows %d, max_tiles %d", batch, q_tile_rows, max_tiles);
+  int64_t qsum = 0, ksum = 0, tiles = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    if (q_lens[b] < 0 || kv_lens[b] < q_lens[b])
+      return fail(ASTR_ERR_INVALID, "request %d: q_len %d, kv_len %d (need 0 <= q_len <= kv_len)", b,
+                  q_lens[b], kv_lens[b]);
+    qsum += q_lens[b];
+    ksum += kv_lens[b];
+    tiles += (q_lens[b] + q_tile_rows - 1) / q_tile_rows;
+  }
+  if (qsum >= (int64_t(1) << 31) || ksum >= (int64_t(1) << 31))
+    return fail(ASTR_ERR_INVALID, "the int32 indptrs cannot hold %lld q rows / %lld keys",
+                (long long)qsum, (long long)ksum);
+  *num_tiles = (int32_t)tiles;
+  if (tiles > max_tiles)
+    return fail(ASTR_ERR_INVALID, "%lld tiles do not fit max_tiles %d", (long long)tiles, max_tiles);
+  if (tiles > 0 && (!q_tile_to_batch || !q_tile_to_index)) return fail(ASTR_ERR_INVALID, "NULL tile maps");
+  qo_indptr[0] = kv_indptr[0] = 0;
+  std::vector<int32_t> tb, ti;
+  std::vector<int64_t> cost;
+  tb.reserve(tiles), ti.reserve(tiles), cost.reserve(tiles);
+  for (int32_t b = 0; b < batch; ++b) {
+    qo_indptr[b + 1] = qo_indptr[b] + q_lens[b];
+    kv_indptr[b + 1] = kv_indptr[b] + kv_lens[b];
+    const int64_t prefix = (int64_t)kv_lens[b] - q_lens[b];
+    for (int32_t t = 0; t * (int64_t)q_tile_rows < q_lens[b]; ++t) {
+      const int64_t last_row = std::min<int64_t>(q_lens[b], (int64_t)(t + 1) * q_tile_rows);
+      tb.push_back(b);
+      ti.push_back(t);
+      cost.push_back((prefix + last_row + 127) / 128);  // 128-key tiles the Q tile visits
+    }
+  }
+  std::vector<int32_t> order(tb.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = (int32_t)i;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] < cost[y]; });
+  for (size_t i = 0; i < order.size(); ++i) {
+    q_tile_to_batch[i] = tb[order[i]];
+    q_tile_to_index[i] = ti[order[i]];
+  }
   return ok();
 }
 
