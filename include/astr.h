@@ -17,6 +17,12 @@
  *    named at each call (and, for decode, the caller's split-K scratch).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t / CUstream handle; NULL is
  *    the legacy default stream). No call synchronises the host unless checked mode is on.
+ *  - CUDA graphs: with checked mode off, every enqueuing call can be stream-captured. Make one
+ *    eager call of each entry point on a device before capturing it there (first calls look up
+ *    device symbols and raise kernel attributes). A captured call keeps the plan it derived
+ *    from its host arguments (batch, max_len, n_tokens, num_q_tiles, split_chunk, the pointers)
+ *    and, for the persistent decode, its work counter; between replays the caller may change
+ *    the contents of the device arrays within those bounds (e.g. seq_lens up to max_len).
  *  - Layouts are row-major and packed: q/k/v rows are [token, head, head_dim] (the pages'
  *    blhd layout with batch and sequence flattened), the cache is
  *    [n_layers, size, n_kv_heads, head_dim], index arrays are int32.
@@ -58,9 +64,11 @@ typedef enum {
 #define ASTR_DEVERR_SLOT 0x1u     /* a slot outside [0, size) */
 #define ASTR_DEVERR_POS 0x2u      /* a position outside [0, freqs_max_len) */
 #define ASTR_DEVERR_ROW 0x4u      /* a req_pool_indices entry outside [0, num_reqs) */
-#define ASTR_DEVERR_LEN 0x8u      /* a length < 1 or beyond max_ctx_len / max_len */
+#define ASTR_DEVERR_LEN 0x8u      /* a length < 1 or beyond max_ctx_len / max_len (bind_tasks:
+                                     a q_len < 0, kv_len < q_len or a sum beyond int32) */
 #define ASTR_DEVERR_TIMEOUT 0x10u /* a bounded wait ran out */
-#define ASTR_DEVERR_META 0x20u    /* checked mode: indptr / tile map inconsistent */
+#define ASTR_DEVERR_META 0x20u    /* checked mode: indptr / tile map inconsistent;
+                                     bind_tasks: the tiles do not fit max_tiles */
 
 /*
  * The pages' KVCache dataclass (inference guide, "KVCache System": "pure data, no methods"),
@@ -215,6 +223,29 @@ astr_status astr_prefill_tiles(const int32_t *q_lens, const int32_t *kv_lens, in
                                int32_t max_tiles, int32_t *num_tiles);
 
 /*
+ * The same per-step metadata computed on the DEVICE, enqueued on `stream` (inference guide,
+ * "KVCache System": bind_tasks() builds the KVCache of a step, its kv_indptr, qo_indptr and
+ * Q-tile maps computed once per step and shared by every layer). For steps captured in a
+ * CUDA graph whose lengths change between replays: the host writes only q_lens / kv_lens.
+ *
+ * q_lens, kv_lens: device int32 [batch]; q_lens may be NULL (a decode batch: only kv_indptr,
+ * the prefix sum of kv_lens = seq_lens, is written, and qo_indptr may be NULL too). Writes
+ * qo_indptr and kv_indptr [batch + 1] and all max_tiles entries of q_tile_to_batch /
+ * q_tile_to_index: the n real tiles in astr_prefill_tiles' order at entries max_tiles - n ..
+ * max_tiles - 1, and -1 in both maps at entries 0 .. max_tiles - n - 1. astr_prefill_attention
+ * skips -1 entries, so it runs on these maps with num_q_tiles = max_tiles, a capacity fixed at
+ * capture. All pointers are device memory owned by the caller. Host-side argument errors
+ * return ASTR_ERR_INVALID (batch above 16383: ASTR_ERR_UNSUPPORTED, the requests held in
+ * shared memory). Device-side: a q_len < 0 or a kv_len < q_len raises ASTR_DEVERR_LEN, more than
+ * max_tiles tiles raises ASTR_DEVERR_META; in both cases every map entry becomes -1 (the
+ * prefill then writes nothing). One launch; each tile's position costs O(batch).
+ */
+astr_status astr_bind_tasks(const int32_t *q_lens, const int32_t *kv_lens, int32_t batch,
+                            int32_t q_tile_rows, int32_t *qo_indptr, int32_t *kv_indptr,
+                            int32_t *q_tile_to_batch, int32_t *q_tile_to_index, int32_t max_tiles,
+                            astr_stream stream);
+
+/*
  * The split plan astr_decode_attention would use for `kv`: chunk length and the number of
  * splits ceil(max_len / chunk). Host-only; enqueues nothing.
  */
@@ -234,12 +265,15 @@ astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *
  * and attends keys j <= P_b + i:
  *   out[t, h, :] = sum_{j <= P_b+i} softmax_j(q[t,h,:] . K_j / sqrt(d)) V_j.
  * The new tokens' K/V (positions P_b..K_b-1) must already be in the cache; kv->n_tokens is
- * the number of packed q rows, qo_indptr[batch] (n_layers * size must stay below 2^31 for the
- * bf16 path, whose row coordinates are 32-bit). Tile t covers
- * request q_tile_to_batch[t], rows [q_tile_rows * q_tile_to_index[t], +q_tile_rows) clipped
- * to Q_b; together the tiles must cover every row exactly once. Rows are written only by
- * their tile. bf16 runs on the tcgen05 tensor cores (bf16 operands, f32 accumulation);
- * f32 runs on the CUDA cores in f32 (no TF32).
+ * the number of rows q and out hold: qo_indptr[batch], or more (a CUDA graph passes its
+ * capacity; rows past qo_indptr[batch] are never written, though a partial last tile may load
+ * and discard some of them). n_layers * size must stay below 2^31 for the bf16 path, whose row
+ * coordinates are 32-bit. Tile t covers request q_tile_to_batch[t], rows
+ * [q_tile_rows * q_tile_to_index[t], +q_tile_rows) clipped to Q_b; together the tiles must
+ * cover every row exactly once. An entry with q_tile_to_batch[t] == -1 is empty and skipped
+ * (astr_bind_tasks pads with these); any other out-of-range entry raises ASTR_DEVERR_META.
+ * Rows are written only by their tile. bf16 runs on the tcgen05 tensor cores (bf16 operands,
+ * f32 accumulation); f32 runs on the CUDA cores in f32 (no TF32).
  * Tile order changes no result. The bf16 kernel starts its blocks from the END of the tile
  * list, so listing tiles in request order runs each request's longest (last) tiles first, and
  * listing them by the number of 128-key tiles they visit, cheapest first, schedules the

@@ -69,6 +69,7 @@ def lib():
             L.astr_decode_attention_rope.argtypes = [KV, I32, P, P, P, I32, P, I32, P, P]
             PI = C.POINTER(I32)
             L.astr_prefill_tiles.argtypes = [PI, PI, I32, I32, PI, PI, PI, PI, I32, PI]
+            L.astr_bind_tasks.argtypes = [P, P, I32, I32, P, P, P, P, I32, P]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
             L.astr_prefill_attention.argtypes = [KV, I32, P, P, I32, P]
             L.astr_last_error.restype = C.c_char_p
@@ -80,7 +81,7 @@ def lib():
             L.astr_kv_cache_bytes.restype = I32
             for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
                          "astr_decode_attention_noalloc", "astr_decode_attention_rope",
-                         "astr_prefill_tiles",
+                         "astr_prefill_tiles", "astr_bind_tasks",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -248,6 +249,23 @@ def astr_prefill_tiles(q_lens, kv_lens, q_tile_rows: int = 128):
     _check(lib().astr_prefill_tiles(ptr(ql), ptr(kl), B, int(q_tile_rows), ptr(qo), ptr(kv), ptr(tb),
                                     ptr(ti), n.value, C.byref(n)))
     return qo, kv, tb[:n.value], ti[:n.value]
+
+
+def astr_bind_tasks(q_lens, kv_lens, qo_indptr, kv_indptr, q_tile_to_batch=None,
+                    q_tile_to_index=None, q_tile_rows: int = 128, stream=None) -> None:
+    """Device-side per-step metadata: fills qo_indptr / kv_indptr and the tile maps (their
+    length is the capacity; unused entries become -1). q_lens None: a decode batch."""
+    import torch
+    for t in (q_lens, kv_lens, qo_indptr, kv_indptr, q_tile_to_batch, q_tile_to_index):
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError("astr_bind_tasks takes int32 tensors")
+    B = int(kv_lens.shape[0])
+    max_tiles = 0 if q_tile_to_batch is None else int(q_tile_to_batch.shape[0])
+    if q_tile_to_index is not None and int(q_tile_to_index.shape[0]) != max_tiles:
+        raise ValueError("q_tile_to_batch and q_tile_to_index differ in length")
+    _check(lib().astr_bind_tasks(_ptr(q_lens), _ptr(kv_lens), B, int(q_tile_rows), _ptr(qo_indptr),
+                                 _ptr(kv_indptr), _ptr(q_tile_to_batch), _ptr(q_tile_to_index),
+                                 max_tiles, _stream(stream)))
 
 
 def astr_decode_plan(kv, n_heads):

@@ -21,15 +21,17 @@ namespace {
 
 // device address of g_error_word on the current device (looked up once per device)
 uint32_t *error_word() {
-  static uint32_t *cache[64] = {};
+  static std::atomic<uint32_t *> cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+  uint32_t *w = cache[dev].load(std::memory_order_acquire);
+  if (!w) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<uint32_t *>(p);
+    w = static_cast<uint32_t *>(p);
+    cache[dev].store(w, std::memory_order_release);
   }
-  return cache[dev];
+  return w;
 }
 
 thread_local std::string t_last_error;
@@ -160,10 +162,10 @@ __global__ void validate_kernel(const astr_kv_cache kv, int what, uint32_t *err)
     if (tid == 0 && kv.kv_indptr && kv.kv_indptr[0] != 0) raise_error(err, ASTR_DEVERR_META);
     return;
   }
-  // prefill: indptr sanity, every tile inside its request, tile count = sum ceil(Q/rows),
-  // and no two tiles naming the same (request, index)
-  __shared__ long long total;
-  if (tid == 0) total = 0;
+  // prefill: indptr sanity, every tile inside its request, non-empty entries = sum
+  // ceil(Q/rows), and no two tiles naming the same (request, index)
+  __shared__ long long total, real;
+  if (tid == 0) total = real = 0;
   __syncthreads();
   long long mine = 0;
   for (int b = tid; b < kv.batch; b += blockDim.x) {
@@ -176,10 +178,12 @@ __global__ void validate_kernel(const astr_kv_cache kv, int what, uint32_t *err)
   }
   atomicAdd(reinterpret_cast<unsigned long long *>(&total), (unsigned long long)mine);
   __syncthreads();
-  if (tid == 0 && (total != kv.num_q_tiles || kv.qo_indptr[0] != 0 || kv.kv_indptr[0] != 0))
-    raise_error(err, ASTR_DEVERR_META);
+  if (tid == 0 && (kv.qo_indptr[0] != 0 || kv.kv_indptr[0] != 0)) raise_error(err, ASTR_DEVERR_META);
+  long long mine_real = 0;
   for (int t = tid; t < kv.num_q_tiles; t += blockDim.x) {
     const int b = kv.q_tile_to_batch[t], i = kv.q_tile_to_index[t];
+    if (b == -1) continue;  // an empty entry
+    ++mine_real;
     if (b < 0 || b >= kv.batch) {
       raise_error(err, ASTR_DEVERR_META);
       continue;
@@ -189,6 +193,9 @@ __global__ void validate_kernel(const astr_kv_cache kv, int what, uint32_t *err)
     for (int u = t + 1; u < kv.num_q_tiles; ++u)
       if (kv.q_tile_to_batch[u] == b && kv.q_tile_to_index[u] == i) raise_error(err, ASTR_DEVERR_META);
   }
+  atomicAdd(reinterpret_cast<unsigned long long *>(&real), (unsigned long long)mine_real);
+  __syncthreads();
+  if (tid == 0 && real != total) raise_error(err, ASTR_DEVERR_META);
 }
 }  // namespace
 
@@ -353,6 +360,27 @@ astr_status astr_prefill_tiles(const int32_t *q_lens, const int32_t *kv_lens, in
     q_tile_to_index[i] = ti[order[i]];
   }
   return ok();
+}
+
+astr_status astr_bind_tasks(const int32_t *q_lens, const int32_t *kv_lens, int32_t batch,
+                            int32_t q_tile_rows, int32_t *qo_indptr, int32_t *kv_indptr,
+                            int32_t *q_tile_to_batch, int32_t *q_tile_to_index, int32_t max_tiles,
+                            astr_stream stream) {
+  if (!kv_indptr || (batch > 0 && !kv_lens) || (q_lens && !qo_indptr))
+    return fail(ASTR_ERR_INVALID, "NULL argument");
+  if (max_tiles > 0 && (!q_tile_to_batch || !q_tile_to_index)) return fail(ASTR_ERR_INVALID, "NULL tile maps");
+  if (batch < 0 || q_tile_rows < 1 || max_tiles < 0)
+    return fail(ASTR_ERR_INVALID, "batch %d, q_tile_rows %d, max_tiles %d", batch, q_tile_rows, max_tiles);
+  if (batch > bind_tasks_max_batch())
+    return fail(ASTR_ERR_UNSUPPORTED, "batch %d above the %d requests the device planner holds", batch,
+                bind_tasks_max_batch());
+  uint32_t *err = error_word();
+  if (!err) return fail(ASTR_ERR_CUDA, "no CUDA device / error word unavailable");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bind_tasks(q_lens, kv_lens, batch, q_tile_rows, qo_indptr, kv_indptr,
+                                    q_tile_to_batch, q_tile_to_index, max_tiles, num_sms(), err, s);
+  if (e != cudaSuccess) return cuda_fail(e, "bind_tasks launch");
+  return finish(s);
 }
 
 astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,

@@ -5,9 +5,28 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/astr.h"
 
 namespace astr {
+
+// ------------------------------------------------------------------------------------------
+// host: a kernel's dynamic shared-memory limit, raised once per device. cudaFuncSetAttribute
+// acts on the current device only, so `done` keeps one bit per device ordinal (< 64) for
+// which it has run. Safe to call from several host threads at once.
+// ------------------------------------------------------------------------------------------
+inline cudaError_t raise_smem_limit_once(const void *kernel, int bytes, std::atomic<uint64_t> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t(1) << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // ------------------------------------------------------------------------------------------
 // device error word (one per device, see astr_device_error); kernels receive its address

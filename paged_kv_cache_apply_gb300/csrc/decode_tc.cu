@@ -744,12 +744,9 @@ template <int G>
 cudaError_t run_g(const DecArgs &a, const CUtensorMap &k16, const CUtensorMap &v16, int64_t grid,
                   cudaStream_t s) {
   auto k = decode_tc_kernel<G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_devices{0};
+  cudaError_t e = raise_smem_limit_once(reinterpret_cast<const void *>(k), kSmemBytes, attr_devices);
+  if (e != cudaSuccess) return e;
   if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, k16, v16);
   return cudaGetLastError();
 }

@@ -56,6 +56,13 @@ cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const v
                               void *out, int32_t n_heads, uint64_t wait_ns, uint32_t *err,
                               cudaStream_t stream);
 
+// per-step metadata on the device (astr_bind_tasks); batch <= bind_tasks_max_batch()
+int bind_tasks_max_batch();
+cudaError_t launch_bind_tasks(const int32_t *q_lens, const int32_t *kv_lens, int32_t batch,
+                              int32_t q_tile_rows, int32_t *qo_indptr, int32_t *kv_indptr,
+                              int32_t *q_tile_to_batch, int32_t *q_tile_to_index,
+                              int32_t max_tiles, int num_sms, uint32_t *err, cudaStream_t stream);
+
 // sets the message astr_last_error() returns on this thread
 void set_last_error_message(const char *msg);
 

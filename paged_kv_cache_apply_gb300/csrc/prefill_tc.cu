@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = a.H / a.Hk;
   const int g = h0 / G;
   const int b = __ldg(a.tile_b + tile);
+  if (b == -1) return;  // an empty entry of the tile list
   if (b < 0 || b >= a.B) {
     if (tid == 0) raise_error(a.err, ASTR_DEVERR_META);
     return;
@@ -442,12 +443,9 @@ struct Maps {
 template <int NQ>
 cudaError_t run_nq(const PreArgs &a, const Maps &m, int64_t grid, cudaStream_t s) {
   auto k = prefill_tc_kernel<NQ>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_devices{0};
+  cudaError_t e = raise_smem_limit_once(reinterpret_cast<const void *>(k), kSmemBytes, attr_devices);
+  if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
   k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, m.q, m.k16, m.v16);
   return cudaGetLastError();

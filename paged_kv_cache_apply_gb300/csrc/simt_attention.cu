@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads) simt_attention_kernel(const AttnArgs
     const int64_t w = blockIdx.x / a.Hk;
     const int tile = (int)(w / a.tile_rows);
     b = __ldg(a.tile_b + tile);
+    if (b == -1) return;  // an empty entry of the tile list
     if (b < 0 || b >= a.B) {
       if (g == 0 && threadIdx.x == 0) raise_error(a.err, ASTR_DEVERR_META);
       return;
