@@ -6,13 +6,17 @@ Uploads the seeded workload (see ``workloads``), runs ``--warmup`` untimed calls
 op, then ``--iters`` calls timed with CUDA events on the current stream, and prints one JSON
 line with the mean time per call. Under a profiler, ``--warmup`` + ``--iters`` is the number of
 launches of the op's kernel (decode: of each of its two kernels when it splits).
+
+``--op bind`` times astr_bind_tasks on the workload's prefill lengths (device q_lens / kv_lens
+to indptrs and tile maps). ``--graph`` captures one call of the op into a CUDA graph after the
+warm-up and times ``--iters`` replays of it instead.
 """
 from __future__ import annotations
 
 import argparse
 import json
 
-OPS = ("rope", "prefill", "decode", "step")
+OPS = ("rope", "prefill", "decode", "step", "bind")
 
 
 def main(argv=None):
@@ -25,8 +29,10 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--no-build", action="store_true", help="load the library as built")
+    ap.add_argument("--graph", action="store_true", help="time replays of a captured call")
     args = ap.parse_args(argv)
 
+    import numpy as np
     import torch
 
     from . import build as B
@@ -37,24 +43,44 @@ def main(argv=None):
         B.build()
     wl = W.make(args.workload)
     dw = DV.DeviceWorkload.upload(wl)
-    run = {"rope": dw.run_rope, "prefill": dw.run_prefill, "decode": dw.run_decode,
-           "step": dw.run_step}[args.op]
-    if args.op == "rope" and dw.rope is None or args.op == "prefill" and dw.prefill is None or \
-            args.op == "decode" and dw.decode is None:
+    if args.op in ("rope", "prefill", "decode", "bind") and \
+            getattr(dw, "prefill" if args.op == "bind" else args.op) is None:
         raise SystemExit(f"workload {wl.name} has no {args.op} call")
+    if args.op == "bind":
+        from . import astr_bind_tasks
+        p = wl.prefill
+        ql = torch.from_numpy(np.diff(p.qo_indptr).astype(np.int32)).cuda()
+        kl = torch.from_numpy(np.diff(p.kv_indptr).astype(np.int32)).cuda()
+        qo, kv = torch.empty(ql.numel() + 1, dtype=torch.int32, device="cuda"), \
+            torch.empty(ql.numel() + 1, dtype=torch.int32, device="cuda")
+        tb = torch.empty(len(p.q_tile_to_batch), dtype=torch.int32, device="cuda")
+        ti = torch.empty_like(tb)
+
+        def run():
+            astr_bind_tasks(ql, kl, qo, kv, tb, ti)
+    else:
+        run = {"rope": dw.run_rope, "prefill": dw.run_prefill, "decode": dw.run_decode,
+               "step": dw.run_step}[args.op]
     for _ in range(args.warmup):
         run()
     torch.cuda.synchronize()
+    call = run
+    if args.graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+            run()
+        call = g.replay
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for _ in range(args.iters):
-        run()
+        call()
     e1.record(s)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / max(args.iters, 1)
-    print(json.dumps({"workload": wl.name, "op": args.op, "iters": args.iters,
-                      "warmup": args.warmup, "ms_per_call": round(ms, 5)}), flush=True)
+    print(json.dumps({"workload": wl.name, "op": args.op, "graph": bool(args.graph),
+                      "iters": args.iters, "warmup": args.warmup, "ms_per_call": round(ms, 5)}),
+          flush=True)
 
 
 if __name__ == "__main__":
