@@ -301,7 +301,7 @@ def tiny_chain(seed: int = SEED_BASE + 1) -> Workload:
     decode2 = DecodeBatch(req_pool_indices=rpi, seq_lens=sl2, kv_indptr=prefix_sum(sl2),
                           max_len=int(sl2.max()), q=None, q_token_offset=0, split_chunk=4,
                           max_splits=4)
-    return Workload("tiny", "1 layer, B=2, H=4, Hk=2, D=64, f32, prefill {7,13} then decode",
+    return Workload("tiny_chain", "1 layer, B=2, H=4, Hk=2, D=64, f32, prefill {7,13} then decode",
                     H, pool, rope=rope, prefill=prefill, rope2=rope2, decode2=decode2,
                     meta={"seed": seed})
 
@@ -324,7 +324,7 @@ def decode_b64_page1(seed: int = SEED_BASE + 2, batch: int = 64, lmin: int = 512
     dec = DecodeBatch(req_pool_indices=rpi, seq_lens=lens, kv_indptr=prefix_sum(lens),
                       max_len=int(lens.max()), q=normal_values((batch, H, D), "bf16", seed, 20),
                       split_chunk=0, max_splits=16)
-    return Workload("decode_b64", f"decode bf16 B={batch} L~U[{lmin},{lmax}] page 1", H, pool,
+    return Workload("decode_b64_page1", f"decode bf16 B={batch} L~U[{lmin},{lmax}] page 1", H, pool,
                     decode=dec, meta={"seed": seed})
 
 
@@ -354,7 +354,7 @@ def prefill_b8_varlen(seed: int = SEED_BASE + 3, batch: int = 8, qmin: int = 256
     pre = PrefillBatch(req_pool_indices=rpi, qo_indptr=prefix_sum(qlens),
                        kv_indptr=prefix_sum(kvl), q_tile_to_batch=tb, q_tile_to_index=ti,
                        q=normal_values((int(qlens.sum()), H, D), "bf16", seed, 20))
-    return Workload("prefill_b8", f"prefill bf16 B={batch} Q~U[{qmin},{qmax}] resumed half",
+    return Workload("prefill_b8_varlen", f"prefill bf16 B={batch} Q~U[{qmin},{qmax}] resumed half",
                     H, pool, prefill=pre, meta={"seed": seed, "prefix": prefix.tolist()})
 
 
