@@ -47,6 +47,8 @@ def lib():
             L.oracle_rope_f64.restype = I
             L.oracle_rope_kv_write.argtypes = [I, I64, I, I, I, P, P, P, P, I, P, P, I64, P, P, P]
             L.oracle_rope_kv_write.restype = I
+            L.oracle_rope_apply.argtypes = [I, I64, I, I, P, P, I, P, I, P]
+            L.oracle_rope_apply.restype = I
             L.oracle_decode.argtypes = [I, I, I, I, I, P, P, P, I64, P, I, I, P, P, I, P, P]
             L.oracle_decode.restype = I
             L.oracle_decode_split.argtypes = [I, I, I, I, I, P, P, P, I64, P, I, I, P, P, I, I,
@@ -125,6 +127,24 @@ def rope_kv_write(q, k, v, freqs, pos, loc, k_layer, v_layer):
     if bad:
         raise ValueError(f"{bad} tokens with a position or slot out of range")
     return q_out
+
+
+def rope_apply(x, freqs, pos, inverse=False):
+    """RoPE with no cache write, under the f32 rounding specification: the rotation by theta
+    (inverse False, the training forward) or by -theta (inverse True: R^T, which maps the
+    gradient of the rotated tensor to the gradient of its input). x: [T, nh, D]."""
+    dt = _dt(x)
+    et = x.dtype
+    x = _c(x, et)
+    fr = _c(freqs, np.float32)
+    pos = _c(pos, np.int32)
+    T, nh, D = x.shape
+    out = np.zeros_like(x)
+    bad = lib().oracle_rope_apply(dt, T, nh, D, _p(x), _p(fr), fr.shape[0], _p(pos),
+                                  1 if inverse else 0, _p(out))
+    if bad:
+        raise ValueError(f"{bad} tokens with a position out of range")
+    return out
 
 
 def _check_layer(k_layer, v_layer, et):

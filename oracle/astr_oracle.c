@@ -4,7 +4,8 @@
  * A plain, slow CPU definition of the paged KV-cache attention path: RoPE applied to Q/K from
  * an f32 [cos, sin] table and written into the cache at out_cache_loc, then GQA
  * softmax(q.k/sqrt(d)).v over the paged cache for decode (optionally split into chunks merged
- * by log-sum-exp) and for varlen causal prefill. Attention is evaluated in double precision
+ * by log-sum-exp) and for varlen causal prefill; on the training path, RoPE with no cache
+ * write and its backward (the rotation by -theta). Attention is evaluated in double precision
  * from the stored (f32 or bf16) values; nothing is blocked, fused or reordered beyond the
  * definitions cited at each function.
  *
@@ -133,19 +134,54 @@ int oracle_rope_f64(int64_t T, int nh, int D, const double *x, const double *fre
   return bad;
 }
 
-/* The same rotation under rounding specification R5 (f32, no fused multiply-add). */
-static void rotate_row_f32(int dtype, const void *src, int64_t src_off, void *dst, int64_t dst_off,
-                           const float *cs, int D) {
+/*
+ * The same rotation under rounding specification R5 (f32, no fused multiply-add). With
+ * `conj` set the table entry is conjugated (c - is): the rotation by -theta, R^T.
+ */
+static void rotate_row_f32_dir(int dtype, const void *src, int64_t src_off, void *dst,
+                               int64_t dst_off, const float *cs, int D, int conj) {
   for (int i = 0; i < D / 2; ++i) {
     float a = load_f32(src, dtype, src_off + 2 * i);
     float b = load_f32(src, dtype, src_off + 2 * i + 1);
-    float c = cs[2 * i], s = cs[2 * i + 1];
+    float c = cs[2 * i], s = conj ? -cs[2 * i + 1] : cs[2 * i + 1];
     float ac = a * c, bs = b * s, as = a * s, bc = b * c;
     float re = ac - bs;
     float im = as + bc;
     store_f32_as(dst, dtype, dst_off + 2 * i, re);
     store_f32_as(dst, dtype, dst_off + 2 * i + 1, im);
   }
+}
+
+static void rotate_row_f32(int dtype, const void *src, int64_t src_off, void *dst, int64_t dst_off,
+                           const float *cs, int D) {
+  rotate_row_f32_dir(dtype, src, src_off, dst, dst_off, cs, D, 0);
+}
+
+/*
+ * RoPE on the training path, with no cache write ([INT-ROPE]: training applies the rotation
+ * as a complex multiply that autograd differentiates; [INF-ROT]: the torch complex path).
+ * For every token t and head h of x [T, nh, D]:
+ *   inverse = 0:  out[t, h] = R_{pos[t]} x[t, h]      (the forward rotation by theta)
+ *   inverse = 1:  out[t, h] = R_{pos[t]}^T x[t, h]    (rotation by -theta)
+ * The rotation is linear in x with the real 2x2 matrix [[c, -s], [s, c]] per pair, so the
+ * gradient of a loss with respect to x is R^T applied to its gradient with respect to out:
+ * inverse = 1 is the backward pass (the complex multiply by the conjugate c - is). Both use
+ * rounding specification R5. A token whose position falls outside the table is skipped and
+ * counted in the return value.
+ */
+int oracle_rope_apply(int dtype, int64_t T, int nh, int D, const void *x, const float *freqs,
+                      int freqs_max_len, const int32_t *pos, int inverse, void *out) {
+  int bad = 0;
+  for (int64_t t = 0; t < T; ++t) {
+    if (pos[t] < 0 || pos[t] >= freqs_max_len) {
+      ++bad;
+      continue;
+    }
+    const float *cs = freqs + (int64_t)pos[t] * D;
+    for (int h = 0; h < nh; ++h)
+      rotate_row_f32_dir(dtype, x, (t * nh + h) * D, out, (t * nh + h) * D, cs, D, inverse);
+  }
+  return bad;
 }
 
 /*
