@@ -160,6 +160,38 @@ astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, con
                                   int32_t n_heads, astr_stream stream);
 
 /*
+ * RoPE on the training path, with no cache write (internals page, "Rotary Position Embedding
+ * (RoPE)": training applies the rotation as a complex multiply that autograd differentiates;
+ * inference guide, "Rotary Embedding Backend": the torch complex path serves training).
+ *
+ * astr_rope_apply, for every token t < n_tokens with p = position_ids[t], (c_i, s_i) =
+ * freqs_cis[p, i] and every pair i:
+ *   q_out[t, h, 2i..2i+1] = rotation of q[t, h, 2i..2i+1] by (c_i, s_i)      (h < n_heads)
+ *   k_out[t, g, 2i..2i+1] = the same rotation of k[t, g, 2i..2i+1]            (g < n_kv_heads)
+ * in the arithmetic of astr_rope_kv_write, whose q_out it reproduces bit for bit.
+ * astr_rope_backward applies the transposed rotation R^T (the complex multiply by the conjugate
+ * c_i - i s_i, i.e. by -theta) to grad_q_out and grad_k_out, giving grad_q and grad_k: the
+ * rotation is linear, so this is its exact backward pass. Its arithmetic is the forward's with
+ * s_i negated: a' = RN(RN(a c) + RN(b s)), b' = RN(RN(b c) - RN(a s)).
+ *
+ * All tensors are DEVICE memory owned by the caller, row-major [n_tokens, heads, head_dim] of
+ * `dtype` (ASTR_F32 or ASTR_BF16), 16-byte aligned; an output may equal its input (in place).
+ * head_dim is 64 or 128 (otherwise ASTR_ERR_UNSUPPORTED). n_kv_heads may be 0 (k and k_out
+ * unused, may be NULL), as may n_heads. freqs_cis is f32 [freqs_max_len, head_dim/2, 2]. A
+ * token whose position is outside [0, freqs_max_len) is skipped and raises ASTR_DEVERR_POS.
+ */
+astr_status astr_rope_apply(const void *q, void *q_out, const void *k, void *k_out,
+                            int64_t n_tokens, int32_t n_heads, int32_t n_kv_heads,
+                            int32_t head_dim, int32_t dtype, const float *freqs_cis,
+                            int32_t freqs_max_len, const int32_t *position_ids,
+                            astr_stream stream);
+astr_status astr_rope_backward(const void *grad_q_out, void *grad_q, const void *grad_k_out,
+                               void *grad_k, int64_t n_tokens, int32_t n_heads,
+                               int32_t n_kv_heads, int32_t head_dim, int32_t dtype,
+                               const float *freqs_cis, int32_t freqs_max_len,
+                               const int32_t *position_ids, astr_stream stream);
+
+/*
  * Decode that allocates nothing. The pages have no counterpart: it exists for callers that
  * cannot call cudaMalloc to provide split-K scratch -- plugin hosts that hand a library only
  * the tensors of one call, embedded runtimes that reserve all device memory at start-up and

@@ -70,6 +70,8 @@ def lib():
             PI = C.POINTER(I32)
             L.astr_prefill_tiles.argtypes = [PI, PI, I32, I32, PI, PI, PI, PI, I32, PI]
             L.astr_bind_tasks.argtypes = [P, P, I32, I32, P, P, P, P, I32, P]
+            L.astr_rope_apply.argtypes = [P, P, P, P, C.c_int64, I32, I32, I32, I32, P, I32, P, P]
+            L.astr_rope_backward.argtypes = [P, P, P, P, C.c_int64, I32, I32, I32, I32, P, I32, P, P]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
             L.astr_prefill_attention.argtypes = [KV, I32, P, P, I32, P]
             L.astr_last_error.restype = C.c_char_p
@@ -81,7 +83,8 @@ def lib():
             L.astr_kv_cache_bytes.restype = I32
             for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
                          "astr_decode_attention_noalloc", "astr_decode_attention_rope",
-                         "astr_prefill_tiles", "astr_bind_tasks",
+                         "astr_prefill_tiles", "astr_bind_tasks", "astr_rope_apply",
+                         "astr_rope_backward",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -221,6 +224,36 @@ def astr_decode_attention_rope(kv, layer_id: int, q, k_new, v_new, n_heads: int,
                                             _ptr(v_new), int(n_heads), _ptr(freqs_cis),
                                             int(freqs_max_len), _ptr(position_ids),
                                             _stream(stream)))
+
+
+def _rope_apply_args(q, q_out, k, k_out, freqs_cis, position_ids):
+    import torch
+    if q.dim() != 3 or q_out.shape != q.shape or q_out.dtype != q.dtype:
+        raise ValueError("q / q_out must both be [n_tokens, n_heads, head_dim] of one dtype")
+    T, H, D = q.shape
+    Hk = 0
+    if k is not None:
+        if k.dim() != 3 or k.shape[0] != T or k.shape[2] != D or k_out is None or \
+                k_out.shape != k.shape or k.dtype != q.dtype or k_out.dtype != q.dtype:
+            raise ValueError("k / k_out must both be [n_tokens, n_kv_heads, head_dim] like q")
+        Hk = k.shape[1]
+    if freqs_cis.dtype != torch.float32 or position_ids.dtype != torch.int32:
+        raise TypeError("freqs_cis must be float32 and position_ids int32")
+    return (_ptr(q), _ptr(q_out), _ptr(k), _ptr(k_out), int(T), int(H), int(Hk), int(D),
+            _dtype_code(q), _ptr(freqs_cis), int(freqs_cis.shape[0]), _ptr(position_ids))
+
+
+def astr_rope_apply(q, q_out, k, k_out, freqs_cis, position_ids, stream=None) -> None:
+    """Training-path RoPE, no cache write: q_out = R q, k_out = R k (k may be None)."""
+    _check(lib().astr_rope_apply(*_rope_apply_args(q, q_out, k, k_out, freqs_cis, position_ids),
+                                 _stream(stream)))
+
+
+def astr_rope_backward(grad_q_out, grad_q, grad_k_out, grad_k, freqs_cis, position_ids,
+                       stream=None) -> None:
+    """The backward of astr_rope_apply: grad_q = R^T grad_q_out, grad_k = R^T grad_k_out."""
+    _check(lib().astr_rope_backward(*_rope_apply_args(grad_q_out, grad_q, grad_k_out, grad_k,
+                                                      freqs_cis, position_ids), _stream(stream)))
 
 
 def astr_decode_attention_noalloc(kv, layer_id, q, n_heads, stream=None) -> None:

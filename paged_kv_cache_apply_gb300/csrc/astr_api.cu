@@ -227,6 +227,39 @@ astr_status decode_impl(const astr_kv_cache *kv, int32_t layer_id, const void *q
 }  // namespace
 }  // namespace astr
 
+namespace astr {
+namespace {
+astr_status rope_apply_impl(const void *q, void *q_out, const void *k, void *k_out,
+                            int64_t n_tokens, int32_t n_heads, int32_t n_kv_heads,
+                            int32_t head_dim, int32_t dtype, const float *freqs_cis,
+                            int32_t freqs_max_len, const int32_t *position_ids, bool inverse,
+                            astr_stream stream, const char *name) {
+  if (n_tokens < 0 || n_heads < 0 || n_kv_heads < 0)
+    return fail(ASTR_ERR_INVALID, "%s: n_tokens %lld, n_heads %d, n_kv_heads %d", name,
+                (long long)n_tokens, n_heads, n_kv_heads);
+  if (dtype != ASTR_F32 && dtype != ASTR_BF16) return fail(ASTR_ERR_INVALID, "%s: dtype %d", name, dtype);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(ASTR_ERR_UNSUPPORTED, "%s: head_dim %d (64 or 128)", name, head_dim);
+  if (n_tokens == 0 || n_heads + n_kv_heads == 0) return ok();
+  if (!freqs_cis || !position_ids || (n_heads > 0 && (!q || !q_out)) ||
+      (n_kv_heads > 0 && (!k || !k_out)))
+    return fail(ASTR_ERR_INVALID, "%s: a NULL tensor", name);
+  if ((n_heads > 0 && (!aligned16(q) || !aligned16(q_out))) ||
+      (n_kv_heads > 0 && (!aligned16(k) || !aligned16(k_out))) || !aligned16(freqs_cis))
+    return fail(ASTR_ERR_INVALID, "%s: tensors and freqs_cis must be 16-byte aligned", name);
+  if (freqs_max_len < 1) return fail(ASTR_ERR_INVALID, "%s: freqs_max_len %d < 1", name, freqs_max_len);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t *err = error_word();
+  if (!err) return fail(ASTR_ERR_CUDA, "no CUDA device / error word unavailable");
+  cudaError_t e = launch_rope_apply(q, q_out, k, k_out, n_tokens, n_heads, n_kv_heads, head_dim,
+                                    dtype, freqs_cis, freqs_max_len, position_ids, inverse, s,
+                                    num_sms(), err);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return finish(s);
+}
+}  // namespace
+}  // namespace astr
+
 using namespace astr;
 
 extern "C" {
@@ -299,6 +332,27 @@ astr_status astr_rope_kv_write(const astr_kv_cache *kv, int32_t layer_id, const 
                                        freqs_max_len, position_ids, s, num_sms(), err);
   if (e != cudaSuccess) return cuda_fail(e, "astr_rope_kv_write launch");
   return finish(s);
+}
+
+
+astr_status astr_rope_apply(const void *q, void *q_out, const void *k, void *k_out,
+                            int64_t n_tokens, int32_t n_heads, int32_t n_kv_heads,
+                            int32_t head_dim, int32_t dtype, const float *freqs_cis,
+                            int32_t freqs_max_len, const int32_t *position_ids,
+                            astr_stream stream) {
+  return astr::rope_apply_impl(q, q_out, k, k_out, n_tokens, n_heads, n_kv_heads, head_dim, dtype,
+                               freqs_cis, freqs_max_len, position_ids, false, stream,
+                               "astr_rope_apply");
+}
+
+astr_status astr_rope_backward(const void *grad_q_out, void *grad_q, const void *grad_k_out,
+                               void *grad_k, int64_t n_tokens, int32_t n_heads,
+                               int32_t n_kv_heads, int32_t head_dim, int32_t dtype,
+                               const float *freqs_cis, int32_t freqs_max_len,
+                               const int32_t *position_ids, astr_stream stream) {
+  return astr::rope_apply_impl(grad_q_out, grad_q, grad_k_out, grad_k, n_tokens, n_heads,
+                               n_kv_heads, head_dim, dtype, freqs_cis, freqs_max_len,
+                               position_ids, true, stream, "astr_rope_backward");
 }
 
 astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *split_chunk,

@@ -14,6 +14,13 @@ cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, cons
                                  const int32_t *position_ids, cudaStream_t stream, int num_sms,
                                  uint32_t *err);
 
+// RoPE with no cache write (training path): the rotation, or its transpose with `inverse`
+cudaError_t launch_rope_apply(const void *q, void *q_out, const void *k, void *k_out,
+                              int64_t n_tokens, int32_t n_heads, int32_t n_kv_heads,
+                              int32_t head_dim, int32_t dtype, const float *freqs,
+                              int32_t freqs_max_len, const int32_t *position_ids, bool inverse,
+                              cudaStream_t stream, int num_sms, uint32_t *err);
+
 // Chunked attention on the CUDA cores: decode (mode 0, one query per request, split into
 // `chunk`-token pieces) or f32 prefill rows (mode 1, one query per packed row, unsplit).
 struct SimtAttnPlan {

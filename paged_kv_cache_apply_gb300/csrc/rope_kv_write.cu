@@ -131,7 +131,105 @@ __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
   }
 }
 
+// RoPE with no cache write (the training path): q_out = R q and k_out = R k, or with Inverse
+// the transposed rotation R^T (the complex multiply by the conjugate entry: s negated), which
+// maps the gradients of the rotated tensors to those of their inputs. One thread per 8-element
+// chunk as above; rows 0..H-1 of a token are query heads, H..H+Hk-1 key heads.
+struct RopeApplyArgs {
+  const void *q;
+  void *q_out;
+  const void *k;
+  void *k_out;
+  const float *freqs;
+  const int32_t *pos;
+  int64_t n_tokens;
+  int32_t freqs_max_len;
+  int32_t H, Hk, D;
+  uint32_t *err;
+};
+
+template <typename T, typename Idx, bool Inverse>
+__global__ void __launch_bounds__(256) rope_apply_kernel(const RopeApplyArgs a) {
+  const int chunk_shift = a.D == 128 ? 4 : 3;
+  const Idx per_token = (Idx)(a.H + a.Hk) << chunk_shift;
+  const Idx total = (Idx)a.n_tokens * per_token;
+  for (Idx id = (Idx)blockIdx.x * blockDim.x + threadIdx.x; id < total;
+       id += (Idx)gridDim.x * blockDim.x) {
+    const Idx tq = id / per_token;
+    const int c = (int)(id - tq * per_token);
+    const int64_t t = (int64_t)tq;
+    const int row = c >> chunk_shift;
+    const int e0 = (c - (row << chunk_shift)) << 3;
+    const int32_t p = __ldg(a.pos + t);
+    if (p < 0 || p >= a.freqs_max_len) {
+      if (c == 0) raise_error(a.err, ASTR_DEVERR_POS);
+      continue;
+    }
+    float cs[8];
+    {
+      const float4 *f =
+          reinterpret_cast<const float4 *>(a.freqs + (int64_t)p * a.D + 2 * (e0 >> 1));
+      float4 f0 = __ldg(f), f1 = __ldg(f + 1);
+      cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+      cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
+    }
+    if (Inverse) cs[1] = -cs[1], cs[3] = -cs[3], cs[5] = -cs[5], cs[7] = -cs[7];
+    float x[8], y[8];
+    if (row < a.H) {
+      const int64_t off = (t * a.H + row) * a.D + e0;
+      Chunk<T>::load(a.q, off, x);
+      rotate4(x, cs, y);
+      Chunk<T>::store(a.q_out, off, y);
+    } else {
+      const int64_t off = (t * a.Hk + (row - a.H)) * a.D + e0;
+      Chunk<T>::load(a.k, off, x);
+      rotate4(x, cs, y);
+      Chunk<T>::store(a.k_out, off, y);
+    }
+  }
+}
+
+template <bool Inverse>
+void launch_apply(const RopeApplyArgs &a, int dtype, int64_t blocks, bool narrow, cudaStream_t s) {
+  if (dtype == ASTR_BF16) {
+    if (narrow) rope_apply_kernel<bf16_t, uint32_t, Inverse><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else rope_apply_kernel<bf16_t, int64_t, Inverse><<<(unsigned)blocks, 256, 0, s>>>(a);
+  } else {
+    if (narrow) rope_apply_kernel<float, uint32_t, Inverse><<<(unsigned)blocks, 256, 0, s>>>(a);
+    else rope_apply_kernel<float, int64_t, Inverse><<<(unsigned)blocks, 256, 0, s>>>(a);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rope_apply(const void *q, void *q_out, const void *k, void *k_out,
+                              int64_t n_tokens, int32_t n_heads, int32_t n_kv_heads,
+                              int32_t head_dim, int32_t dtype, const float *freqs,
+                              int32_t freqs_max_len, const int32_t *position_ids, bool inverse,
+                              cudaStream_t stream, int num_sms, uint32_t *err) {
+  RopeApplyArgs a;
+  a.q = q;
+  a.q_out = q_out;
+  a.k = k;
+  a.k_out = k_out;
+  a.freqs = freqs;
+  a.pos = position_ids;
+  a.n_tokens = n_tokens;
+  a.freqs_max_len = freqs_max_len;
+  a.H = n_heads;
+  a.Hk = n_kv_heads;
+  a.D = head_dim;
+  a.err = err;
+  const int64_t total = n_tokens * (int64_t)(n_heads + n_kv_heads) * (head_dim / 8);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)num_sms * 32;
+  if (blocks > cap) blocks = cap;
+  const bool narrow = total + blocks * 256 < (int64_t(1) << 32);
+  if (inverse) launch_apply<true>(a, dtype, blocks, narrow, stream);
+  else launch_apply<false>(a, dtype, blocks, narrow, stream);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, const void *q,
                                  void *q_out, const void *k, const void *v, int32_t n_heads,
