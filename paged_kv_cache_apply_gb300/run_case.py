@@ -7,7 +7,8 @@ op, then ``--iters`` calls timed with CUDA events on the current stream, and pri
 line with the mean time per call. Under a profiler, ``--warmup`` + ``--iters`` is the number of
 launches of the op's kernel (decode: of each of its two kernels when it splits).
 
-``--op bind`` times astr_bind_tasks on the workload's prefill lengths (device q_lens / kv_lens
+``--op rope_backward`` times astr_rope_backward on the rope step's q and k (the gradients of
+the training path have the same shapes). ``--op bind`` times astr_bind_tasks on the workload's prefill lengths (device q_lens / kv_lens
 to indptrs and tile maps). ``--graph`` captures one call of the op into a CUDA graph after the
 warm-up and times ``--iters`` replays of it instead.
 """
@@ -16,7 +17,7 @@ from __future__ import annotations
 import argparse
 import json
 
-OPS = ("rope", "prefill", "decode", "step", "bind")
+OPS = ("rope", "prefill", "decode", "step", "bind", "rope_backward")
 
 
 def main(argv=None):
@@ -43,8 +44,8 @@ def main(argv=None):
         B.build()
     wl = W.make(args.workload)
     dw = DV.DeviceWorkload.upload(wl)
-    if args.op in ("rope", "prefill", "decode", "bind") and \
-            getattr(dw, "prefill" if args.op == "bind" else args.op) is None:
+    need = {"bind": "prefill", "rope_backward": "rope"}.get(args.op, args.op)
+    if need != "step" and getattr(dw, need) is None:
         raise SystemExit(f"workload {wl.name} has no {args.op} call")
     if args.op == "bind":
         from . import astr_bind_tasks
@@ -58,6 +59,13 @@ def main(argv=None):
 
         def run():
             astr_bind_tasks(ql, kl, qo, kv, tb, ti)
+    elif args.op == "rope_backward":
+        from . import astr_rope_backward
+        r = dw.rope
+        gq, gk = torch.empty_like(r["q"]), torch.empty_like(r["k"])
+
+        def run():
+            astr_rope_backward(r["q"], gq, r["k"], gk, r["freqs"], r["pos"])
     else:
         run = {"rope": dw.run_rope, "prefill": dw.run_prefill, "decode": dw.run_decode,
                "step": dw.run_step}[args.op]
