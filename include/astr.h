@@ -57,7 +57,8 @@ typedef enum {
   ASTR_ERR_UNSUPPORTED = 2, /* valid but not implemented: head_dim, dtype, group size */
   ASTR_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
   ASTR_ERR_INDEX = 4,       /* checked mode: a kernel met an out-of-range index */
-  ASTR_ERR_TIMEOUT = 5      /* checked mode: a kernel wait ran out of time */
+  ASTR_ERR_TIMEOUT = 5,     /* checked mode: a kernel wait ran out of time */
+  ASTR_ERR_NO_SPACE = 6     /* page pool: not enough free or evictable pages */
 } astr_status;
 
 /* bits of the per-device error word */
@@ -313,6 +314,56 @@ astr_status astr_decode_plan(const astr_kv_cache *kv, int32_t n_heads, int32_t *
  */
 astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
                                    void *out, int32_t n_heads, astr_stream stream);
+
+/*
+ * Paged-pool bookkeeping on the HOST (inference guide, "KVCache System": PagePool over a
+ * bitmask page allocator with ref-counts and LRU eviction, and RadixCache, exact page-aligned
+ * prefix matching; internals page, "Cache Architecture"). Enqueues no GPU work; every call
+ * takes the pool's mutex.
+ *
+ * Page p owns the token slots [p * page_size, (p + 1) * page_size) of the flat KV buffers, so a
+ * request whose pages are pg[0..] has slot pg[j / page_size] * page_size + j % page_size at
+ * position j of its req_to_token row. A page is free, referenced (held by requests: ref > 0) or
+ * cached without a reference. The radix cache holds complete pages only, as edges from a parent
+ * prefix labelled by the page's exact token tuple: a page is shared only under the same parent
+ * prefix, and the hash each entry keeps (astr_pool_page_info) never decides a match. With
+ * page_size 1 there is no prefix sharing: match finds nothing and record keeps nothing.
+ *
+ * astr_pool_match: the longest run of complete pages of tokens[0..n_tokens) cached along one
+ *   path from the root, at most max_pages; writes them to pages[0..*n_matched) and takes a
+ *   reference on each (they cannot be evicted until released). A request resumes prefill after
+ *   *n_matched * page_size tokens; to keep at least one row to compute, pass n_tokens = prompt
+ *   length - 1.
+ * astr_pool_alloc: n fresh pages (ref 1), the lowest free page numbers first. When too few are
+ *   free, unreferenced cached leaves are evicted least recently used first (match and record
+ *   count as uses), a parent becoming a leaf in turn. ASTR_ERR_NO_SPACE if that is not enough
+ *   (pages evicted on the way stay evicted; nothing is allocated).
+ * astr_pool_record: enter the complete pages of tokens[0..n_materialized) -- the tokens whose
+ *   K/V are in the cache: on completion the prompt plus the generated tokens except the last
+ *   sampled one -- with the request's pages[0..n_pages) (pages[i] holds tokens i * page_size..).
+ *   Where the path already has an edge with the same tuple, the cached page is kept and the
+ *   request's own copy stays private (freed when released). The partial last page is never
+ *   entered. The caller must hold a reference on every page it passes; a page already cached on
+ *   another path, or passed twice, is rejected (ASTR_ERR_INVALID, nothing changed).
+ * astr_pool_release: drop one reference per entry of pages[0..n) (repeats drop several). A page
+ *   left with no reference is freed if it is not cached, or becomes evictable once it is a
+ *   cached leaf. Releasing a reference not held is ASTR_ERR_INVALID and changes nothing.
+ * astr_pool_stats / astr_pool_page_info: counts (free, cached, evictable) and one page's
+ *   reference count, whether it is cached and its entry's hash (0 when not cached).
+ */
+typedef struct astr_page_pool astr_page_pool;
+astr_status astr_pool_create(int32_t n_pages, int32_t page_size, astr_page_pool **pool);
+astr_status astr_pool_destroy(astr_page_pool *pool);
+astr_status astr_pool_match(astr_page_pool *pool, const int32_t *tokens, int64_t n_tokens,
+                            int32_t max_pages, int32_t *pages, int32_t *n_matched);
+astr_status astr_pool_alloc(astr_page_pool *pool, int32_t n, int32_t *pages);
+astr_status astr_pool_record(astr_page_pool *pool, const int32_t *tokens, int64_t n_materialized,
+                             const int32_t *pages, int32_t n_pages);
+astr_status astr_pool_release(astr_page_pool *pool, const int32_t *pages, int32_t n);
+astr_status astr_pool_stats(astr_page_pool *pool, int32_t *free_pages, int32_t *cached_pages,
+                            int32_t *evictable_pages);
+astr_status astr_pool_page_info(astr_page_pool *pool, int32_t page, int32_t *refs,
+                                int32_t *cached, uint64_t *hash);
 
 /* Message of the last failing call on this host thread ("" if none). */
 const char *astr_last_error(void);

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libastr.so")
 
 ASTR_F32, ASTR_BF16 = 0, 1
 STATUS = {0: "ASTR_OK", 1: "ASTR_ERR_INVALID", 2: "ASTR_ERR_UNSUPPORTED", 3: "ASTR_ERR_CUDA",
-          4: "ASTR_ERR_INDEX", 5: "ASTR_ERR_TIMEOUT"}
+          4: "ASTR_ERR_INDEX", 5: "ASTR_ERR_TIMEOUT", 6: "ASTR_ERR_NO_SPACE"}
 DEVERR_SLOT, DEVERR_POS, DEVERR_ROW, DEVERR_LEN, DEVERR_TIMEOUT, DEVERR_META = 1, 2, 4, 8, 16, 32
 
 
@@ -70,6 +70,15 @@ def lib():
             PI = C.POINTER(I32)
             L.astr_prefill_tiles.argtypes = [PI, PI, I32, I32, PI, PI, PI, PI, I32, PI]
             L.astr_bind_tasks.argtypes = [P, P, I32, I32, P, P, P, P, I32, P]
+            PP = C.c_void_p
+            L.astr_pool_create.argtypes = [I32, I32, C.POINTER(PP)]
+            L.astr_pool_destroy.argtypes = [PP]
+            L.astr_pool_match.argtypes = [PP, PI, C.c_int64, I32, PI, PI]
+            L.astr_pool_alloc.argtypes = [PP, I32, PI]
+            L.astr_pool_record.argtypes = [PP, PI, C.c_int64, PI, I32]
+            L.astr_pool_release.argtypes = [PP, PI, I32]
+            L.astr_pool_stats.argtypes = [PP, PI, PI, PI]
+            L.astr_pool_page_info.argtypes = [PP, I32, PI, PI, C.POINTER(C.c_uint64)]
             L.astr_rope_apply.argtypes = [P, P, P, P, C.c_int64, I32, I32, I32, I32, P, I32, P, P]
             L.astr_rope_backward.argtypes = [P, P, P, P, C.c_int64, I32, I32, I32, I32, P, I32, P, P]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
@@ -84,7 +93,9 @@ def lib():
             for name in ["astr_rope_kv_write", "astr_decode_attention", "astr_decode_plan",
                          "astr_decode_attention_noalloc", "astr_decode_attention_rope",
                          "astr_prefill_tiles", "astr_bind_tasks", "astr_rope_apply",
-                         "astr_rope_backward",
+                         "astr_rope_backward", "astr_pool_create", "astr_pool_destroy",
+                         "astr_pool_match", "astr_pool_alloc", "astr_pool_record",
+                         "astr_pool_release", "astr_pool_stats", "astr_pool_page_info",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -299,6 +310,81 @@ def astr_bind_tasks(q_lens, kv_lens, qo_indptr, kv_indptr, q_tile_to_batch=None,
     _check(lib().astr_bind_tasks(_ptr(q_lens), _ptr(kv_lens), B, int(q_tile_rows), _ptr(qo_indptr),
                                  _ptr(kv_indptr), _ptr(q_tile_to_batch), _ptr(q_tile_to_index),
                                  max_tiles, _stream(stream)))
+
+
+class PagePool:
+    """The host page pool of libastr: a bitmask page allocator with reference counts and LRU
+    eviction, and a radix cache of complete token pages (astr_pool_* in include/astr.h).
+    Arguments and results are int32 numpy arrays / Python ints; page p owns the slots
+    [p * page_size, (p + 1) * page_size)."""
+
+    def __init__(self, n_pages: int, page_size: int):
+        self.page_size = int(page_size)
+        h = C.c_void_p()
+        _check(lib().astr_pool_create(int(n_pages), self.page_size, C.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().astr_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _i32(a):
+        import numpy as np
+        return np.ascontiguousarray(a, dtype=np.int32)
+
+    @staticmethod
+    def _p(a):
+        return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+    def match(self, tokens, max_pages=None):
+        """Pages of the longest cached complete-page prefix of tokens (each now referenced)."""
+        import numpy as np
+        t = self._i32(tokens)
+        mp = t.size // self.page_size if max_pages is None else int(max_pages)
+        out = np.zeros(max(mp, 1), np.int32)
+        n = C.c_int32(0)
+        _check(lib().astr_pool_match(self._h, self._p(t), t.size, mp, self._p(out), C.byref(n)))
+        return out[:n.value].copy()
+
+    def alloc(self, n: int):
+        import numpy as np
+        out = np.zeros(max(int(n), 1), np.int32)
+        _check(lib().astr_pool_alloc(self._h, int(n), self._p(out)))
+        return out[:int(n)].copy()
+
+    def record(self, tokens, n_materialized: int, pages):
+        t, p = self._i32(tokens), self._i32(pages)
+        _check(lib().astr_pool_record(self._h, self._p(t), int(n_materialized), self._p(p), p.size))
+
+    def release(self, pages):
+        p = self._i32(pages)
+        _check(lib().astr_pool_release(self._h, self._p(p), p.size))
+
+    def stats(self):
+        """(free pages, cached pages, evictable pages)."""
+        a, b, c = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(lib().astr_pool_stats(self._h, C.byref(a), C.byref(b), C.byref(c)))
+        return a.value, b.value, c.value
+
+    def page_info(self, page: int):
+        """(references, cached, entry hash) of one page."""
+        r, c, h = C.c_int32(), C.c_int32(), C.c_uint64()
+        _check(lib().astr_pool_page_info(self._h, int(page), C.byref(r), C.byref(c), C.byref(h)))
+        return r.value, bool(c.value), h.value
+
+    def slots(self, pages, n_tokens: int):
+        """The req_to_token row entries of positions 0..n_tokens-1 held in `pages`."""
+        import numpy as np
+        j = np.arange(int(n_tokens))
+        return (self._i32(pages)[j // self.page_size] * self.page_size + j % self.page_size).astype(np.int32)
 
 
 def astr_decode_plan(kv, n_heads):

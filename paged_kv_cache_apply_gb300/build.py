@@ -1,4 +1,4 @@
-"""Build libastr.so (sm_103a) in-tree with nvcc: one object per .cu, compiled in parallel."""
+"""Build libastr.so (sm_103a) in-tree with nvcc: one object per .cu / .cpp, compiled in parallel."""
 from __future__ import annotations
 
 import glob
@@ -36,7 +36,7 @@ def _stale(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
                      glob.glob(os.path.join(ROOT, "include", "*.h")))
 
