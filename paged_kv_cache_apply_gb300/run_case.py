@@ -7,6 +7,10 @@ op, then ``--iters`` calls timed with CUDA events on the current stream, and pri
 line with the mean time per call. Under a profiler, ``--warmup`` + ``--iters`` is the number of
 launches of the op's kernel (decode: of each of its two kernels when it splits).
 
+``--op pool`` times the host page pool (no GPU): ``--iters`` request lifecycles of 1024 shared
+system-prompt tokens plus 512 tokens of their own, page 16, each a match, an allocation, a
+record of its tokens and a release, on a 65536-page pool.
+
 ``--op rope_backward`` times astr_rope_backward on the rope step's q and k (the gradients of
 the training path have the same shapes). ``--op bind`` times astr_bind_tasks on the workload's prefill lengths (device q_lens / kv_lens
 to indptrs and tile maps). ``--graph`` captures one call of the op into a CUDA graph after the
@@ -17,7 +21,7 @@ from __future__ import annotations
 import argparse
 import json
 
-OPS = ("rope", "prefill", "decode", "step", "bind", "rope_backward")
+OPS = ("rope", "prefill", "decode", "step", "bind", "rope_backward", "pool")
 
 
 def main(argv=None):
@@ -34,6 +38,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
 
     import numpy as np
+
+    if args.op == "pool":
+        return _time_pool(args)
     import torch
 
     from . import build as B
@@ -89,6 +96,41 @@ def main(argv=None):
     print(json.dumps({"workload": wl.name, "op": args.op, "graph": bool(args.graph),
                       "iters": args.iters, "warmup": args.warmup, "ms_per_call": round(ms, 5)}),
           flush=True)
+
+
+def _time_pool(args):
+    import time
+
+    import numpy as np
+
+    from . import PagePool
+    from . import build as B
+    if not args.no_build:
+        B.build()
+    ps, shared, own = 16, 1024, 512
+    pool = PagePool(65536, ps)
+    rng = np.random.default_rng(7)
+    system = rng.integers(0, 32000, shared)
+    reqs = [np.concatenate([system, rng.integers(0, 32000, own)]).astype(np.int32)
+            for _ in range(args.iters + args.warmup)]
+    hits = 0
+
+    def life(toks):
+        hit = pool.match(toks[:-1])
+        pages = np.concatenate([hit, pool.alloc((len(toks) + ps - 1) // ps - len(hit))])
+        pool.record(toks, len(toks), pages)
+        pool.release(pages)
+        return len(hit)
+
+    for t in reqs[:args.warmup]:
+        life(t)
+    t0 = time.perf_counter()
+    for t in reqs[args.warmup:]:
+        hits += life(t)
+    us = (time.perf_counter() - t0) / max(args.iters, 1) * 1e6
+    print(json.dumps({"op": "pool", "iters": args.iters, "tokens_per_request": shared + own,
+                      "page_size": ps, "mean_hit_pages": round(hits / max(args.iters, 1), 1),
+                      "us_per_request": round(us, 2), "stats": pool.stats()}), flush=True)
 
 
 if __name__ == "__main__":
