@@ -196,11 +196,31 @@ class DeviceWorkload:
         d = getattr(self, which)
         astr_decode_attention(self._c(d), d["layer"], d["q"], self.n_heads, stream)
 
-    def run_step(self, stream=None):
-        """One pass of the path over the batch: rotate + write, then prefill, then decode."""
+    def run_step(self, stream=None, side_stream=None):
+        """One pass of the path over the batch: rotate + write, then prefill, then decode.
+
+        With `side_stream` (a torch.cuda.Stream) the prefill runs there, concurrently with the
+        decode on the main stream (`stream`, a torch.cuda.Stream, else the current one): both
+        only read what the rotate + write produced and write disjoint outputs. The main stream
+        waits for the prefill before the step ends."""
+        if side_stream is None or self.prefill is None or self.decode is None:
+            if self.rope is not None:
+                self.run_rope("rope", stream)
+            if self.prefill is not None:
+                self.run_prefill(stream)
+            if self.decode is not None:
+                self.run_decode("decode", stream)
+            return
+        import torch
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if not hasattr(self, "_step_events"):
+            self._step_events = (torch.cuda.Event(), torch.cuda.Event())
+        written, prefilled = self._step_events
         if self.rope is not None:
-            self.run_rope("rope", stream)
-        if self.prefill is not None:
-            self.run_prefill(stream)
-        if self.decode is not None:
-            self.run_decode("decode", stream)
+            self.run_rope("rope", main.cuda_stream)
+        written.record(main)
+        side_stream.wait_event(written)
+        self.run_prefill(side_stream.cuda_stream)
+        self.run_decode("decode", main.cuda_stream)
+        prefilled.record(side_stream)
+        main.wait_event(prefilled)
