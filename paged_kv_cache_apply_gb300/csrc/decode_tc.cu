@@ -10,8 +10,9 @@
 // kernel is persistent: one block per SM claims items from a counter until none are left, and
 // its copy pipeline streams from one item into the next without draining, so a block's
 // start-up (3.5 us before its first tile) is paid once per SM instead of once per item:
-//  * warp 9 claims items (split-major: every request's first chunk before any second one, so
-//    the long chunks go first), publishes each through a two-slot ring in shared memory, and
+//  * warp 9 claims items (split-major: every request's first chunk before any second one, and
+//    within a split the requests longest first, so the run ends on the shortest chunks),
+//    publishes each through a two-slot ring in shared memory, and
 //    stages the item's query rows in one of two Q buffers;
 //  * warps 4-7 stream 128-token tiles of the item's KV-head slices of K and V into a 3-stage
 //    ring in the 128-byte-swizzled operand layout, 32 tokens per warp: when those are two
@@ -67,7 +68,9 @@ constexpr int kOffLsum = kOffRed + 2 * 4 * 16 * 4;    // [4 warps][16] f32
 constexpr int kOffBar = kOffLsum + 4 * 16 * 4;
 constexpr int kOffRing = kOffBar + 32 * 8;            // 2 published work items, 64 bytes each
 constexpr int kOffMisc = kOffRing + 2 * 64;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;      // + alignment slack
+constexpr int kSortMax = 1024;                        // batches up to this size claim longest first
+constexpr int kOffOrder = kOffMisc + 64;              // [kSortMax] requests by seq_len, then scratch
+constexpr int kSmemBytes = kOffOrder + 2 * kSortMax * 4 + 1024;  // + alignment slack
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kNPad, false, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, kNPad, true, false);
@@ -244,6 +247,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {  // zero both Q and both P buffers (rows past the group stay zero)
     uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
     for (int i = tid; i < (8192 + 8192) / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
+  }
+  // Requests ranked by seq_len, longest first (ties by index): the claims walk the ranks within
+  // each split, so every split's long chunks go first and the run ends on the shortest ones.
+  int32_t *order = reinterpret_cast<int32_t *>(smem + kOffOrder);
+  const bool ranked = a.B <= kSortMax;
+  if (ranked) {
+    int32_t *lens = order + kSortMax;
+    for (int b = tid; b < a.B; b += kThreads) lens[b] = __ldg(a.seq_lens + b);
+    __syncthreads();
+    for (int b = tid; b < a.B; b += kThreads) {
+      const int32_t L = lens[b];
+      int r = 0;
+      for (int u = 0; u < a.B; ++u) {
+        const int32_t Lu = lens[u];
+        r += (Lu > L) | ((Lu == L) & (u < b));
+      }
+      order[r] = b;  // the ranks are a permutation of 0..B-1
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -484,9 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ============ scheduler: claims items, publishes them, stages their query rows ============
-    // Work positions are split-major (every request's first chunk before any second one), so
-    // the long chunks go first. Block c starts at position c; each further position comes from
-    // the counter once the other roles have taken the block's previous item.
+    // Work positions are split-major (every request's first chunk before any second one) and,
+    // within a split, follow the requests' seq_len ranks, so the long chunks go first and the
+    // run ends on the short ones. Block c starts at position c; each further position comes
+    // from the counter once the other roles have taken the block's previous item.
     const int64_t per_split = (int64_t)a.B * a.Hk;
     auto claim = [&]() -> int64_t {
       unsigned got = 0;
@@ -502,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (pos < a.n_items) {
         w.split = (int)(pos / per_split);
         const int rest = (int)(pos % per_split);
-        w.b = rest / a.Hk;
+        w.b = ranked ? order[rest / a.Hk] : rest / a.Hk;
         w.g = rest % a.Hk;
         w.L = __ldg(a.seq_lens + w.b);
         bool good = true;
@@ -683,6 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           have_prev = true;
           prev_ob = ob;
           prev_first = j == 0;
+        }
+        // the item's last P.V goes in now rather than after the next item's first S: its stage
+        // frees sooner and the epilogue, which waits for it, overlaps the next item's loads
+        if (ok && have_prev) {
+          ok = pv(it - 1, prev_ob, prev_first);
+          have_prev = false;
         }
       }
       if (ok && have_prev && !pv(it - 1, prev_ob, prev_first)) ok = false;
