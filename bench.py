@@ -451,8 +451,11 @@ def run_gpu(args):
                        "frac_hbm": round(dec_gbs / hbm, 4)},
             "serialised_step": {"ms": round(serial_ms, 5)},
         },
-        "roofline": {"kernel": "astr_decode_attention call: decode_tc_kernel partials + "
-                               "split_merge_kernel (timed together, traffic of both)",
+        "roofline": {"kernel": ("astr_decode_attention call: decode_tc_kernel partials + "
+                                "split_merge_kernel (timed together, traffic of both)")
+                               if n_splits > 1 else
+                               "astr_decode_attention call: decode_tc_kernel, requests unsplit "
+                               "(no merge launched)",
                      "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm, 4), "traffic": traffic,

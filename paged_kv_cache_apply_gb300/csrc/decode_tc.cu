@@ -787,6 +787,7 @@ bool tc_decode_supported(int dtype, int head_dim, int group) {
 }
 
 int tc_decode_tile_tokens() { return kTok; }
+int tc_decode_ranked_batch_max() { return kSortMax; }
 
 cudaError_t launch_tc_decode(const astr_kv_cache &kv, int32_t layer_id, const void *q,
                              int32_t n_heads, const SimtAttnPlan &plan, cudaStream_t stream,

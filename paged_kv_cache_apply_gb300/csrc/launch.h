@@ -44,6 +44,7 @@ cudaError_t launch_split_merge(const astr_kv_cache &kv, int32_t n_heads, const S
 // tcgen05 bf16 decode (head_dim 128)
 bool tc_decode_supported(int dtype, int head_dim, int group);
 int tc_decode_tile_tokens();
+int tc_decode_ranked_batch_max();  // batches up to this size claim their requests longest first
 // RoPE and the new token's cache write folded into the decode (astr_decode_attention_rope)
 struct DecodeRope {
   const void *k_new;
