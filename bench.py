@@ -279,7 +279,7 @@ def run_gpu(args):
     side = torch.cuda.Stream()  # the prefill runs here, concurrently with the decode
 
     for _ in range(args.warmup):
-        dw.run_step(side_stream=side)
+        dw.run_step(side_stream=side, fused=True)
     torch.cuda.synchronize()
 
     K = args.steps
@@ -310,7 +310,7 @@ def run_gpu(args):
     wall0 = time.time()
     t_start.record(stream)
     for i in range(K):  # the step: events at the two ends only (an event between kernels costs)
-        dw.run_step(side_stream=side)
+        dw.run_step(side_stream=side, fused=True)
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.mark(wall0, time.time())
@@ -375,7 +375,7 @@ def run_gpu(args):
         if i >= 2:
             stream.wait_event(out_free[x])  # step i-2's outputs have been read back
         dw.rope, dw.prefill, dw.decode = bind[x]
-        dw.run_step(side_stream=side)
+        dw.run_step(side_stream=side, fused=True)
         step_done[x].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(step_done[x])
@@ -436,8 +436,10 @@ def run_gpu(args):
                         "freqs max_len 8192",
             "l2": "no flush: each step reads ~2.2 GB of K/V (> 129 MB L2)",
             "parallelism": f"replicas x{world}",
-            "streams": "rope + write, then the prefill on a second stream concurrently with the "
-                       "decode; the step ends when both are done",
+            "streams": "second stream: rope + write of the 2048 prefill tokens, then the prefill; "
+                       "main stream, concurrently: the decode with the rope + write of its 256 "
+                       "new tokens folded in (astr_decode_attention_rope); the step ends when "
+                       "both are done",
             "timing": "rows and roofline: K steps with the ops serialised and an event between "
                       "them; then value: K steps with CUDA events at the ends only",
             "decode_split_chunk": chunk, "decode_splits": n_splits,

@@ -10,7 +10,8 @@ from typing import Optional
 
 import numpy as np
 
-from . import (KVCache, astr_decode_attention, astr_prefill_attention, astr_rope_kv_write)
+from . import (KVCache, astr_decode_attention, astr_decode_attention_rope,
+               astr_prefill_attention, astr_rope_kv_write)
 from .workloads import Workload
 
 
@@ -179,12 +180,15 @@ class DeviceWorkload:
                         setattr(kv, name, new)
 
     def refresh(self):
+        self.__dict__.pop("_fused_cache", None)  # holds slices and structs of the old tensors
         for d in [self.rope, self.rope2, self.prefill, self.decode, self.decode2]:
             if d is not None:
                 d.pop("c", None)
 
     def run_rope(self, which="rope", stream=None):
-        r = getattr(self, which)
+        self.run_rope_dict(getattr(self, which), stream)
+
+    def run_rope_dict(self, r, stream=None):
         astr_rope_kv_write(self._c(r), r["layer"], r["q"], r["q_out"], r["k"], r["v"],
                            self.n_heads, r["freqs"], r["freqs"].shape[0], r["pos"], stream)
 
@@ -196,13 +200,56 @@ class DeviceWorkload:
         d = getattr(self, which)
         astr_decode_attention(self._c(d), d["layer"], d["q"], self.n_heads, stream)
 
-    def run_step(self, stream=None, side_stream=None):
+    def _fused_parts(self):
+        """For a step whose decode tokens lead the rope batch: the rope of the prefill tokens
+        alone, and the decode call with the decode tokens' rotation and cache write folded in."""
+        import dataclasses
+        key = (id(self.rope), id(self.prefill), id(self.decode))
+        cache = self.__dict__.setdefault("_fused_cache", {})
+        if key not in cache:
+            r, d, n = self.rope, self.decode, self.wl.decode.batch
+            rp = {k: (v[n:] if k in ("q", "q_out", "k", "v", "pos", "loc") else v)
+                  for k, v in r.items() if k not in ("kv", "c")}
+            rp["kv"] = KVCache(self.k_buffer, self.v_buffer, out_cache_loc=rp["loc"])
+            dk = dataclasses.replace(d["kv"], out_cache_loc=r["loc"][:n])
+            cache[key] = (rp, dk.as_c(), (r["q"][:n], r["k"][:n], r["v"][:n], r["pos"][:n]))
+        return cache[key]
+
+    def fusable(self):
+        """Whether run_step(fused=True) applies: decode tokens first in the rope batch, the
+        prefill's rows right after them, and both queries taken from the rotated q."""
+        w = self.wl
+        return (self.rope is not None and self.prefill is not None and self.decode is not None and
+                w.decode.q is None and w.decode.q_token_offset == 0 and w.prefill.q is None and
+                w.prefill.q_token_offset == w.decode.batch)
+
+    def run_step(self, stream=None, side_stream=None, fused=False):
         """One pass of the path over the batch: rotate + write, then prefill, then decode.
 
         With `side_stream` (a torch.cuda.Stream) the prefill runs there, concurrently with the
         decode on the main stream (`stream`, a torch.cuda.Stream, else the current one): both
         only read what the rotate + write produced and write disjoint outputs. The main stream
-        waits for the prefill before the step ends."""
+        waits for the prefill before the step ends. With `fused` as well (see fusable()), the
+        decode rotates and writes its own new tokens (astr_decode_attention_rope) and the side
+        stream rotates and writes only the prefill tokens before the prefill, so neither waits
+        for the other; the results are the same bytes."""
+        if fused and side_stream is not None and self.fusable():
+            import torch
+            main = stream if stream is not None else torch.cuda.current_stream()
+            if not hasattr(self, "_step_events"):
+                self._step_events = (torch.cuda.Event(), torch.cuda.Event())
+            begun, prefilled = self._step_events
+            rp, dec_c, (q, k_new, v_new, pos) = self._fused_parts()
+            begun.record(main)  # the side stream starts after whatever preceded the step
+            side_stream.wait_event(begun)
+            self.run_rope_dict(rp, side_stream.cuda_stream)
+            self.run_prefill(side_stream.cuda_stream)
+            d = self.decode
+            astr_decode_attention_rope(dec_c, d["layer"], q, k_new, v_new, self.n_heads, rp["freqs"],
+                                       rp["freqs"].shape[0], pos, main.cuda_stream)
+            prefilled.record(side_stream)
+            main.wait_event(prefilled)
+            return
         if side_stream is None or self.prefill is None or self.decode is None:
             if self.rope is not None:
                 self.run_rope("rope", stream)
