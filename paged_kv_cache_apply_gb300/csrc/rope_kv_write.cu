@@ -131,6 +131,53 @@ __global__ void __launch_bounds__(256) rope_kv_write_kernel(const RopeArgs a) {
   }
 }
 
+// The same work with one block per token: the block's threads take the token's chunks (a
+// stride loop when there are more chunks than threads), so the position and slot are read once
+// per block and no chunk index is divided to find its token.
+template <typename T>
+__global__ void __launch_bounds__(512) rope_kv_write_token_kernel(const RopeArgs a) {
+  const int64_t t = blockIdx.x;
+  const int chunk_shift = a.D == 128 ? 4 : 3;
+  const int per_token = (a.H + 2 * a.Hk) << chunk_shift;
+  const int32_t p = __ldg(a.pos + t);
+  const int32_t s = __ldg(a.loc + t);
+  const bool pos_ok = p >= 0 && p < a.freqs_max_len;
+  const bool slot_ok = s >= 0 && (int64_t)s < a.size;
+  if (!(pos_ok && slot_ok)) {
+    if (threadIdx.x == 0) raise_error(a.err, (pos_ok ? 0u : ASTR_DEVERR_POS) | (slot_ok ? 0u : ASTR_DEVERR_SLOT));
+    return;
+  }
+  for (int c = threadIdx.x; c < per_token; c += blockDim.x) {
+    const int row = c >> chunk_shift;
+    const int e0 = (c - (row << chunk_shift)) << 3;
+    if (row >= a.H + a.Hk) {  // value head: copied unchanged
+      const int g = row - a.H - a.Hk;
+      Chunk<T>::copy(a.v, (t * a.Hk + g) * a.D + e0, a.v_layer, ((int64_t)s * a.Hk + g) * a.D + e0);
+      continue;
+    }
+    float cs[8];
+    {
+      const float4 *f =
+          reinterpret_cast<const float4 *>(a.freqs + (int64_t)p * a.D + 2 * (e0 >> 1));
+      float4 f0 = __ldg(f), f1 = __ldg(f + 1);
+      cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+      cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
+    }
+    float x[8], y[8];
+    if (row < a.H) {
+      const int64_t off = (t * a.H + row) * a.D + e0;
+      Chunk<T>::load(a.q, off, x);
+      rotate4(x, cs, y);
+      Chunk<T>::store(a.q_out, off, y);
+    } else {
+      const int g = row - a.H;
+      Chunk<T>::load(a.k, (t * a.Hk + g) * a.D + e0, x);
+      rotate4(x, cs, y);
+      Chunk<T>::store(a.k_layer, ((int64_t)s * a.Hk + g) * a.D + e0, y);
+    }
+  }
+}
+
 // RoPE with no cache write (the training path): q_out = R q and k_out = R k, or with Inverse
 // the transposed rotation R^T (the complex multiply by the conjugate entry: s negated), which
 // maps the gradients of the rotated tensors to those of their inputs. One thread per 8-element
@@ -257,6 +304,15 @@ cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, cons
   a.err = err;
   const int64_t total = kv.n_tokens * (int64_t)(n_heads + 2 * kv.n_kv_heads) * (kv.head_dim / 8);
   if (total == 0) return cudaSuccess;
+  if (kv.n_tokens <= INT32_MAX) {  // a block per token
+    const int64_t per_token = (int64_t)(n_heads + 2 * kv.n_kv_heads) * (kv.head_dim / 8);
+    const int threads = per_token >= 512 ? 512 : (int)((per_token + 31) / 32 * 32);
+    if (kv.dtype == ASTR_BF16)
+      rope_kv_write_token_kernel<bf16_t><<<(unsigned)kv.n_tokens, threads, 0, stream>>>(a);
+    else
+      rope_kv_write_token_kernel<float><<<(unsigned)kv.n_tokens, threads, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)num_sms * 32;
   if (blocks > cap) blocks = cap;
