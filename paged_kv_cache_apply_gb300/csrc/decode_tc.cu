@@ -69,8 +69,9 @@ constexpr int kOffBar = kOffLsum + 4 * 16 * 4;
 constexpr int kOffRing = kOffBar + 32 * 8;            // 2 published work items, 64 bytes each
 constexpr int kOffMisc = kOffRing + 2 * 64;
 constexpr int kSortMax = 1024;                        // batches up to this size claim longest first
-constexpr int kOffOrder = kOffMisc + 64;              // [kSortMax] requests by seq_len, then scratch
-constexpr int kSmemBytes = kOffOrder + 2 * kSortMax * 4 + 1024;  // + alignment slack
+constexpr int kBuckets = 1024;                        // seq_len ranks by 128-token tile count
+constexpr int kOffOrder = kOffMisc + 64;              // [kSortMax] requests by seq_len, [kBuckets] counts
+constexpr int kSmemBytes = kOffOrder + (kSortMax + kBuckets) * 4 + 1024;  // + alignment slack
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kNPad, false, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, kNPad, true, false);
@@ -248,22 +249,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4 *z = reinterpret_cast<uint4 *>(smem + kOffQ);
     for (int i = tid; i < (8192 + 8192) / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
   }
-  // Requests ranked by seq_len, longest first (ties by index): the claims walk the ranks within
-  // each split, so every split's long chunks go first and the run ends on the shortest ones.
+  // Requests ranked by seq_len in 128-token tiles, most tiles first (ties by index): the claims
+  // walk the ranks within each split, so every split's long chunks go first and the run ends on
+  // the shortest ones. A stable counting sort: a histogram of tile counts, a descending exclusive
+  // scan over it, and a placement in index order. It must be deterministic: every block ranks
+  // for itself, and the claim counter they share only means the same request to all of them if
+  // their ranks agree.
   int32_t *order = reinterpret_cast<int32_t *>(smem + kOffOrder);
   const bool ranked = a.B <= kSortMax;
   if (ranked) {
-    int32_t *lens = order + kSortMax;
-    for (int b = tid; b < a.B; b += kThreads) lens[b] = __ldg(a.seq_lens + b);
+    int32_t *cnt = order + kSortMax;  // [kBuckets]: counts, then the next free rank of each
+    __shared__ int32_t warp_sums[kThreads / 32];
+    auto bucket = [](int32_t L) {
+      const int32_t t = L > 0 ? (L + 127) >> 7 : 0;
+      return t < kBuckets ? t : kBuckets - 1;
+    };
+    for (int k = tid; k < kBuckets; k += kThreads) cnt[k] = 0;
     __syncthreads();
-    for (int b = tid; b < a.B; b += kThreads) {
-      const int32_t L = lens[b];
-      int r = 0;
-      for (int u = 0; u < a.B; ++u) {
-        const int32_t Lu = lens[u];
-        r += (Lu > L) | ((Lu == L) & (u < b));
+    for (int b = tid; b < a.B; b += kThreads) atomicAdd(&cnt[bucket(__ldg(a.seq_lens + b))], 1);
+    __syncthreads();
+    // thread i holds buckets kBuckets-1-4i .. kBuckets-4-4i (descending); scan their sums
+    constexpr int kPer = (kBuckets + kThreads - 1) / kThreads;
+    int local[kPer], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int rv = tid * kPer + j;
+      local[j] = rv < kBuckets ? cnt[kBuckets - 1 - rv] : 0;
+      sum += local[j];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += warp_sums[w];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int rv = tid * kPer + j;
+      if (rv < kBuckets) cnt[kBuckets - 1 - rv] = run;  // first rank of that bucket
+      run += local[j];
+    }
+    __syncthreads();
+    if (warp == 0) {  // 32 requests at a time, in index order; lanes sharing a count take turns
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        const bool live = b < a.B;
+        const int k = live ? bucket(__ldg(a.seq_lens + b)) : -1 - lane;  // unique for dead lanes
+        const unsigned same = __match_any_sync(0xffffffffu, k);
+        const int before = __popc(same & ((1u << lane) - 1u));
+        const int base = live ? cnt[k] : 0;
+        __syncwarp();
+        if (live) {
+          order[base + before] = b;
+          if (before == 0) cnt[k] = base + __popc(same);
+        }
+        __syncwarp();
       }
-      order[r] = b;  // the ranks are a permutation of 0..B-1
     }
   }
   tc::fence_before_sync();
