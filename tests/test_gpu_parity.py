@@ -367,3 +367,30 @@ def test_empty_batches_are_no_ops():
     _sync()
     assert torch.equal(before.view(torch.int16), dw.decode["out"].view(torch.int16))
     del kv2
+
+
+@pytest.mark.parametrize("B,lens_kind", [(1100, "varied"), (1024, "ties")])
+def test_decode_large_batches_rank_or_not(B, lens_kind):
+    # up to 1024 requests the persistent decode ranks them by length (ties by index) and may
+    # leave them unsplit; beyond that it claims them in index order. Both must cover every
+    # request exactly once.
+    rng = np.random.default_rng(B)
+    if lens_kind == "ties":
+        lens = rng.choice([100, 128, 129, 256, 700], B).astype(np.int32)  # many equal tile counts
+    else:
+        lens = rng.integers(1, 600, B).astype(np.int32)
+    wl = W.make_case("bf16", 16, 4, 128, 16, lens, None, n_layers=1, layer_id=0, split_chunk=0,
+                     max_splits=16, seed=W.SEED_BASE + 1300 + B)
+    dw = DV.DeviceWorkload.upload(wl)
+    dw.decode["out"].zero_()
+    dw.run_decode()
+    _sync()
+    d = wl.decode
+    sel = np.sort(rng.choice(B, 96, replace=False)).astype(np.int32)
+    ref = oracle.decode(d.q, wl.pool.k_buffer[0], wl.pool.v_buffer[0], wl.pool.req_to_token,
+                        d.req_pool_indices, d.seq_lens, sel=sel)
+    got = DV.to_host(dw.decode["out"])
+    assert maxerr(got[sel], ref[sel]) <= TOL["bf16"]
+    # and no request was skipped: every output row was written (zeroed before the call)
+    assert np.all(np.any(got.reshape(B, -1) != 0, axis=1))
+    assert A.astr_device_error() == 0
