@@ -244,9 +244,30 @@ def cpu_baseline(wl, dec_fraction, pre_fraction, repeats=1, min_seconds=10.0):
     desc = (f"rope+write of all {wl.rope.n_tokens} tokens, prefill of "
             f"{'all' if prows is None else len(prows)} of {wl.prefill.total_q} rows, decode of "
             f"{'all' if dsel is None else len(dsel)} of {wl.decode.batch} requests")
-    return {"value": work["total_bytes"] / dt / 1e9, "unit": "GB/s",
-            "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
-            "seconds_per_sample": round(dt, 4), "repeats": repeats}
+    out = {"value": work["total_bytes"] / dt / 1e9, "unit": "GB/s",
+           "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+           "seconds_per_sample": round(dt, 4), "repeats": repeats}
+    # the same oracle on one host thread, over a 1/16 sample of the decode requests and prefill rows
+    threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        d1, p1 = oracle_sample(wl, dec_fraction / 16, pre_fraction / 16)
+        w1 = step_work(wl, d1, p1)
+        t0 = time.perf_counter()
+        run_oracle_step(wl, kl, vl, d1, p1)
+        one = time.perf_counter() - t0
+        reps = max(1, min(20, int(math.ceil(min_seconds / 2 / max(one, 1e-3)))))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            run_oracle_step(wl, kl, vl, d1, p1)
+        dt1 = (time.perf_counter() - t0) / reps
+        out["single_thread"] = {"value": w1["total_bytes"] / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                                "sample": f"rope+write of all {wl.rope.n_tokens} tokens, prefill of "
+                                          f"{len(p1)} rows, decode of {len(d1)} requests",
+                                "seconds_per_sample": round(dt1, 4), "repeats": reps}
+    finally:
+        oracle.set_num_threads(threads)
+    return out
 
 
 # ---------------------------------------------------------------------------------------------
