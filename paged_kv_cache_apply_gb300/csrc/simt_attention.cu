@@ -399,7 +399,10 @@ __global__ void __launch_bounds__(kThreads) simt_attention_kernel(const AttnArgs
   }
 }
 
-// Log-sum-exp merge of the split-K partials: one warp per (request, head).
+// Log-sum-exp merge of the split-K partials: one warp per (request, head). The maximum and the
+// weights are taken with the lanes spread over the splits; the weighted partials are then
+// summed split by split, eight splits' loads in flight at a time (a warp that waited on each
+// split's loads in turn spent most of a many-split merge on memory latency).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) split_merge_kernel(const AttnArgs a) {
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -411,21 +414,35 @@ __global__ void __launch_bounds__(256) split_merge_kernel(const AttnArgs a) {
   const int n = (L + a.chunk - 1) / a.chunk;
   if (n <= 1) return;  // written directly by the attention kernel
   const int64_t base = ((int64_t)b * a.H + h) * a.max_splits;
+  const float2 *ml = reinterpret_cast<const float2 *>(a.ml_part) + base;  // (m, l) per split
   float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, a.ml_part[(base + s) * 2]);
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, ml[s].x);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int PER = D / 32;
   float o[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) o[e] = 0.f;
-  float den = 0.f;
-  for (int s = 0; s < n; ++s) {
-    const float w = a.ml_part[(base + s) * 2 + 1] *
-                    ex2_approx((a.ml_part[(base + s) * 2] - M) * 1.4426950408889634f);
-    den += w;
-    const float *op = a.o_part + (base + s) * D + lane * PER;
+  float den_part = 0.f;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    float w_mine = 0.f;  // the weight of split s0 + lane
+    if (s0 + lane < n) {
+      const float2 v = ml[s0 + lane];
+      w_mine = v.y * ex2_approx((v.x - M) * 1.4426950408889634f);
+    }
+    den_part += w_mine;
+    const int cnt = n - s0 < 32 ? n - s0 : 32;
+#pragma unroll 8
+    for (int j = 0; j < cnt; ++j) {
+      const float w = __shfl_sync(0xffffffffu, w_mine, j);
+      const float *op = a.o_part + (base + s0 + j) * D + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) o[e] += w * op[e];
+      for (int e = 0; e < PER; ++e) o[e] += w * op[e];
+    }
   }
+  float den = den_part;
+#pragma unroll
+  for (int o2 = 16; o2 >= 1; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
   const float inv = 1.f / den;
 #pragma unroll
   for (int e = 0; e < PER; ++e) Elem<T>::store_out(a.out, ((int64_t)b * a.H + h) * D + lane * PER + e, o[e] * inv);
