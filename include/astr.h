@@ -152,10 +152,14 @@ astr_status astr_rope_kv_write(const astr_kv_cache *kv, int32_t layer_id, const 
  * ceil(max_len / C) <= max_splits; the scratch may be NULL only when every request fits in
  * one chunk (C >= max_len). kv_indptr is not read (checked mode verifies it equals the prefix
  * sum of seq_lens).
+ * With split_chunk 0 the library may also leave every request in one chunk (C = max_len,
+ * nothing merged) when the batch alone balances the GPU.
  * The bf16 head_dim-128 kernel is persistent: one block per SM takes (request, chunk, KV
- * head) items from a work counter in device memory that belongs to the library. Each call uses
- * the next of 32 such counters on the current device (its last block resets it), so calls
- * overlapping on different streams stay independent unless 32 of them run at once.
+ * head) items from a work counter in device memory that belongs to the library, chunk by
+ * chunk and, for batches up to 1024, each chunk's requests longest first (the order moves work
+ * between SMs and changes no result). Each call uses the next of 32 such counters on the
+ * current device (its last block resets it), so calls overlapping on different streams stay
+ * independent unless 32 of them run at once.
  */
 astr_status astr_decode_attention(const astr_kv_cache *kv, int32_t layer_id, const void *q,
                                   int32_t n_heads, astr_stream stream);
