@@ -70,22 +70,23 @@ def test_forward_reproduces_rope_kv_write_q_out():
     assert torch.equal(q_out.view(torch.int16), r["q_out"].view(torch.int16))
 
 
-def test_autograd_function_runs_both_passes_in_the_library():
+@pytest.mark.parametrize("dt,D", [("bf16", 128), ("f32", 64)])
+def test_autograd_function_runs_both_passes_in_the_library(dt, D):
     import torch
     from paged_kv_cache_apply_gb300.rotary import apply_rotary_emb
-    Bn, L, H, Hk, D = 2, 50, 8, 2, 128
-    seed = W.SEED_BASE + 1100
-    qh = W.normal_values((Bn * L, H, D), "bf16", seed, 1)
-    kh = W.normal_values((Bn * L, Hk, D), "bf16", seed, 2)
-    gqh = W.normal_values((Bn * L, H, D), "bf16", seed, 3)
-    gkh = W.normal_values((Bn * L, Hk, D), "bf16", seed, 4)
+    Bn, L, H, Hk = 2, 50, 8, 2
+    seed = W.SEED_BASE + 1100 + D
+    qh = W.normal_values((Bn * L, H, D), dt, seed, 1)
+    kh = W.normal_values((Bn * L, Hk, D), dt, seed, 2)
+    gqh = W.normal_values((Bn * L, H, D), dt, seed, 3)
+    gkh = W.normal_values((Bn * L, Hk, D), dt, seed, 4)
     fr = W.rope_freqs_cis(256, D)
     pos = np.tile(np.arange(L, dtype=np.int32), Bn)
-    q = _dev(qh, "bf16").view(Bn, L, H, D).detach().requires_grad_(True)
-    k = _dev(kh, "bf16").view(Bn, L, Hk, D).detach().requires_grad_(True)
+    q = _dev(qh, dt).view(Bn, L, H, D).detach().requires_grad_(True)
+    k = _dev(kh, dt).view(Bn, L, Hk, D).detach().requires_grad_(True)
     qr, kr = apply_rotary_emb(q, k, _dev(fr, "f32"), _dev(pos, "i32").view(Bn, L))
-    torch.autograd.backward([qr, kr], [_dev(gqh, "bf16").view(Bn, L, H, D),
-                                       _dev(gkh, "bf16").view(Bn, L, Hk, D)])
+    torch.autograd.backward([qr, kr], [_dev(gqh, dt).view(Bn, L, H, D),
+                                       _dev(gkh, dt).view(Bn, L, Hk, D)])
     torch.cuda.synchronize()
     assert np.array_equal(DV.to_host(qr.detach().reshape(-1, H, D)), oracle.rope_apply(qh, fr, pos))
     assert np.array_equal(DV.to_host(kr.detach().reshape(-1, Hk, D)), oracle.rope_apply(kh, fr, pos))

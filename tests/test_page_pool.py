@@ -110,3 +110,41 @@ def test_argument_errors():
     with pytest.raises(A.AstrError):
         pool.page_info(4)
     assert list(pool.slots([3, 1], 6)) == [12, 13, 14, 15, 4, 5]
+
+
+def test_concurrent_threads_keep_the_pool_consistent():
+    # every call takes the pool's mutex: four threads running request lifecycles at once must
+    # leave every page accounted for
+    import threading
+    ps, n_pages = 4, 256
+    pool = A.PagePool(n_pages, ps)
+    base = [7] * (8 * ps)
+    errors = []
+
+    def worker(seed):
+        rng = np.random.default_rng(seed)
+        try:
+            for _ in range(300):
+                toks = base[:int(rng.integers(0, 8 * ps))] + [int(x) for x in rng.integers(0, 3, 6)]
+                hit = list(pool.match(toks[:-1]))
+                try:
+                    new = list(pool.alloc((len(toks) + ps - 1) // ps - len(hit)))
+                except A.AstrError as e:
+                    assert e.status == 6
+                    pool.release(hit)
+                    continue
+                pages = hit + new
+                pool.record(toks, len(toks) - 1, pages)
+                pool.release(pages)
+        except Exception as e:  # surfaced below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(s,)) for s in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]
+    free, cached, evictable = pool.stats()
+    held = sum(pool.page_info(p)[0] > 0 for p in range(n_pages))
+    assert held == 0 and free + cached == n_pages and evictable <= cached
