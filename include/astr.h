@@ -72,8 +72,9 @@ typedef enum {
                                      bind_tasks: the tiles do not fit max_tiles */
 
 /*
- * The pages' KVCache dataclass (inference guide, "KVCache System": "pure data, no methods"),
- * as plain device pointers and host sizes. Fields a call does not use may be NULL / 0.
+ * The pages' KVCache dataclass (inference guide, "KVCache System": a plain data record
+ * without methods), as plain device pointers and host sizes. Fields a call does not use may be
+ * NULL / 0.
  */
 typedef struct astr_kv_cache {
   /* KVStorage: flat token-level buffers [n_layers, size, n_kv_heads, head_dim] of `dtype` */

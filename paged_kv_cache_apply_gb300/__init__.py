@@ -139,7 +139,7 @@ def _dtype_code(t) -> int:
 
 @dataclass
 class KVCache:
-    """The pages' ``KVCache`` dataclass over torch device tensors ("pure data, no methods").
+    """The pages' ``KVCache`` dataclass over torch device tensors (a plain data record without methods).
 
     ``k_buffer``/``v_buffer``: [n_layers, size, n_kv_heads, head_dim]; every index tensor is
     int32. ``max_len`` is a host int. Unused fields stay None.
