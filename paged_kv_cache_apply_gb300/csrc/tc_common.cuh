@@ -155,6 +155,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_saddr, const void *map,
       : "memory");
 }
 
+// ---- TMA tensor store: one 2-D box from shared memory to `map` at (x = column, y = row); the
+// issuing thread commits its stores as a bulk group and waits until their sources are read ------
+__device__ __forceinline__ void tma_store_2d(const void *map, int x, int y, uint32_t src_saddr) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src_saddr)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ---- Ampere-style async copies (16 bytes, zero-filled when src_bytes = 0) -----------------
 __device__ __forceinline__ void cp_async16(uint32_t dst_saddr, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_saddr), "l"(src),
