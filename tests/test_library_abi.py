@@ -97,6 +97,49 @@ def test_decode_plan_host_only(L):
     assert (chunk.value, n.value) == (50, 1)
 
 
+def _sms():
+    # the planner asks the current device for its SM count and assumes 148 without one
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return 148
+
+
+def _plan_rule(batch, Hk, max_len, max_splits, tc=True):
+    """The library's automatic split plan (decode_chunk in csrc/astr_api.cu), restated: whole
+    requests (no split) when the tensor-core kernel
+    ranks the batch (<= 1024 requests) and batch x n_kv_heads >= 6 x SMs; otherwise about four
+    items per SM (tensor-core kernel) or four waves of three blocks per SM (CUDA-core kernel)
+    from a mean length of max_len / 2, within [512 or 256, 4096] tokens, no more splits than
+    max_splits, rounded up to whole 128-token (tensor-core) tiles, and at most max_len."""
+    sms = _sms()
+    if tc and batch <= 1024 and batch * Hk >= 6 * sms:
+        return max_len, 1
+    c = (batch * max_len // 2) * Hk // (sms * (4 if tc else 12))
+    c = max(c, 512 if tc else 256)
+    c = min(c, 4096)
+    c = max(c, -(-max_len // max_splits))
+    c = -(-c // 128) * 128 if tc else c
+    c = min(c, max_len)
+    return c, -(-max_len // c)
+
+
+@pytest.mark.parametrize("batch,Hk,max_len,max_splits", [
+    (256, 4, 8192, 16), (64, 4, 4096, 16), (4, 4, 131072, 32), (1, 4, 600, 8), (2000, 4, 8192, 8),
+    (300, 1, 1 << 20, 512),
+])
+def test_decode_plan_follows_the_stated_rule(L, batch, Hk, max_len, max_splits):
+    c = _fake_cache(head_dim=128, n_kv_heads=Hk, batch=batch, max_len=max_len, max_ctx_len=max_len,
+                    decode_o_part=0x40000, decode_ml_part=0x50000, max_splits=max_splits)
+    chunk, n = C.c_int32(), C.c_int32()
+    assert L.astr_decode_plan(C.byref(c), 4 * Hk, C.byref(chunk), C.byref(n)) == 0
+    assert (chunk.value, n.value) == _plan_rule(batch, Hk, max_len, max_splits)
+    assert n.value <= max_splits and chunk.value * n.value >= max_len
+
+
 def test_prefill_and_rope_reject_bad_arguments(L):
     c = _fake_cache(qo_indptr=0x1000, kv_indptr=0x1000, q_tile_to_batch=0x1000,
                     q_tile_to_index=0x1000, num_q_tiles=2, q_tile_rows=64)
