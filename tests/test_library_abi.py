@@ -109,12 +109,13 @@ def _sms():
 
 
 def _plan_rule(batch, Hk, max_len, max_splits, tc=True):
-    """The library's automatic split plan (decode_chunk in csrc/astr_api.cu), restated: whole
-    requests (no split) when the tensor-core kernel
-    ranks the batch (<= 1024 requests) and batch x n_kv_heads >= 6 x SMs; otherwise about four
-    items per SM (tensor-core kernel) or four waves of three blocks per SM (CUDA-core kernel)
-    from a mean length of max_len / 2, within [512 or 256, 4096] tokens, no more splits than
-    max_splits, rounded up to whole 128-token (tensor-core) tiles, and at most max_len."""
+    """The library's automatic split plan (decode_chunk in csrc/astr_api.cu), restated.
+
+    Whole requests (no split) when the tensor-core kernel ranks the batch (<= 1024 requests)
+    and batch x n_kv_heads >= 6 x SMs. Otherwise about four items per SM (tensor-core kernel)
+    or four waves of three blocks per SM (CUDA-core kernel) from a mean length of max_len / 2,
+    within [512 or 256, 4096] tokens, no more splits than max_splits, rounded up to whole
+    128-token tiles (tensor-core kernel), and at most max_len."""
     sms = _sms()
     if tc and batch <= 1024 and batch * Hk >= 6 * sms:
         return max_len, 1
