@@ -108,23 +108,21 @@ def _sms():
     return 148
 
 
-def _plan_rule(batch, Hk, max_len, max_splits, tc=True):
-    """The library's automatic split plan (decode_chunk in csrc/astr_api.cu), restated.
+def _plan_rule(batch, Hk, max_len, max_splits):
+    """The library's automatic split plan for the tensor-core decode kernel (decode_chunk in
+    csrc/astr_api.cu), restated.
 
-    Whole requests (no split) when the tensor-core kernel ranks the batch (<= 1024 requests)
-    and batch x n_kv_heads >= 6 x SMs. Otherwise about four items per SM (tensor-core kernel)
-    or four waves of three blocks per SM (CUDA-core kernel) from a mean length of max_len / 2,
-    within [512 or 256, 4096] tokens, no more splits than max_splits, rounded up to whole
-    128-token tiles (tensor-core kernel), and at most max_len."""
+    Whole requests (no split) when the kernel ranks the batch (<= 1024 requests) and
+    batch x n_kv_heads >= 6 x SMs. Otherwise about four items per SM from a mean length of
+    max_len / 2, within [512, 4096] tokens, no more splits than max_splits, rounded up to whole
+    128-token tiles, and at most max_len."""
     sms = _sms()
-    if tc and batch <= 1024 and batch * Hk >= 6 * sms:
+    if batch <= 1024 and batch * Hk >= 6 * sms:
         return max_len, 1
-    c = (batch * max_len // 2) * Hk // (sms * (4 if tc else 12))
-    c = max(c, 512 if tc else 256)
-    c = min(c, 4096)
+    c = (batch * max_len // 2) * Hk // (sms * 4)
+    c = min(max(c, 512), 4096)
     c = max(c, -(-max_len // max_splits))
-    c = -(-c // 128) * 128 if tc else c
-    c = min(c, max_len)
+    c = min(-(-c // 128) * 128, max_len)
     return c, -(-max_len // c)
 
 
