@@ -211,7 +211,9 @@ astr_status astr_rope_backward(const void *grad_q_out, void *grad_q, const void 
  * on a device looks up the array's device address (cudaGetSymbolAddress); make that first
  * call before any stream capture. Every call shares the array and it keeps the last call's
  * contents; no entry has to start at zero because each call writes every entry it reads.
- * Calls whose work overlaps on the GPU (several streams) race on the array.
+ * Calls whose work overlaps on the GPU (several streams) race on the array. The looked-up
+ * address is kept for the life of the process: after a device reset (cudaDeviceReset, or a
+ * reset of the primary context) it is stale, so do not call this entry point again after one.
  */
 astr_status astr_decode_attention_noalloc(const astr_kv_cache *kv, int32_t layer_id,
                                           const void *q, int32_t n_heads, astr_stream stream);
@@ -355,6 +357,10 @@ astr_status astr_prefill_attention(const astr_kv_cache *kv, int32_t layer_id, co
  *   cached leaf. Releasing a reference not held is ASTR_ERR_INVALID and changes nothing.
  * astr_pool_stats / astr_pool_page_info: counts (free, cached, evictable) and one page's
  *   reference count, whether it is cached and its entry's hash (0 when not cached).
+ * astr_pool_slots: the req_to_token row entries of positions 0..n_tokens-1 for a request
+ *   holding pages[0..n_pages): slots[j] = pages[j / page_size] * page_size + j % page_size.
+ *   ASTR_ERR_INVALID (nothing written past the failing entry) when the pages cannot hold
+ *   n_tokens or a page number is outside the pool. Reads no pool state beyond its size.
  */
 typedef struct astr_page_pool astr_page_pool;
 astr_status astr_pool_create(int32_t n_pages, int32_t page_size, astr_page_pool **pool);
@@ -369,6 +375,8 @@ astr_status astr_pool_stats(astr_page_pool *pool, int32_t *free_pages, int32_t *
                             int32_t *evictable_pages);
 astr_status astr_pool_page_info(astr_page_pool *pool, int32_t page, int32_t *refs,
                                 int32_t *cached, uint64_t *hash);
+astr_status astr_pool_slots(astr_page_pool *pool, const int32_t *pages, int32_t n_pages,
+                            int64_t n_tokens, int32_t *slots);
 
 /* Message of the last failing call on this host thread ("" if none). */
 const char *astr_last_error(void);

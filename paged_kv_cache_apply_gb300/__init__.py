@@ -79,6 +79,7 @@ def lib():
             L.astr_pool_release.argtypes = [PP, PI, I32]
             L.astr_pool_stats.argtypes = [PP, PI, PI, PI]
             L.astr_pool_page_info.argtypes = [PP, I32, PI, PI, C.POINTER(C.c_uint64)]
+            L.astr_pool_slots.argtypes = [PP, PI, I32, C.c_int64, PI]
             L.astr_rope_apply.argtypes = [P, P, P, P, C.c_int64, I32, I32, I32, I32, P, I32, P, P]
             L.astr_rope_backward.argtypes = [P, P, P, P, C.c_int64, I32, I32, I32, I32, P, I32, P, P]
             L.astr_decode_plan.argtypes = [KV, I32, C.POINTER(I32), C.POINTER(I32)]
@@ -95,7 +96,7 @@ def lib():
                          "astr_prefill_tiles", "astr_bind_tasks", "astr_rope_apply",
                          "astr_rope_backward", "astr_pool_create", "astr_pool_destroy",
                          "astr_pool_match", "astr_pool_alloc", "astr_pool_record",
-                         "astr_pool_release", "astr_pool_stats", "astr_pool_page_info",
+                         "astr_pool_release", "astr_pool_stats", "astr_pool_page_info", "astr_pool_slots",
                          "astr_prefill_attention", "astr_set_checked", "astr_set_wait_timeout_ns",
                          "astr_device_error", "astr_selftest_wait_timeout"]:
                 getattr(L, name).restype = I32
@@ -383,8 +384,10 @@ class PagePool:
     def slots(self, pages, n_tokens: int):
         """The req_to_token row entries of positions 0..n_tokens-1 held in `pages`."""
         import numpy as np
-        j = np.arange(int(n_tokens))
-        return (self._i32(pages)[j // self.page_size] * self.page_size + j % self.page_size).astype(np.int32)
+        p = self._i32(pages)
+        out = np.zeros(max(int(n_tokens), 1), np.int32)
+        _check(lib().astr_pool_slots(self._h, self._p(p), p.size, int(n_tokens), self._p(out)))
+        return out[:int(n_tokens)].copy()
 
 
 def astr_decode_plan(kv, n_heads):

@@ -311,4 +311,21 @@ astr_status astr_pool_page_info(astr_page_pool *pool, int32_t page, int32_t *ref
   return pool_ok();
 }
 
+astr_status astr_pool_slots(astr_page_pool *pool, const int32_t *pages, int32_t n_pages,
+                            int64_t n_tokens, int32_t *slots) {
+  if (!pool || n_tokens < 0 || n_pages < 0 || (n_tokens > 0 && (!pages || !slots)))
+    return pool_fail(ASTR_ERR_INVALID, "astr_pool_slots: bad argument");
+  const int64_t ps = pool->page_size;
+  if (n_tokens > (int64_t)n_pages * ps)
+    return pool_fail(ASTR_ERR_INVALID, "astr_pool_slots: the pages cannot hold n_tokens tokens");
+  // the page table is not read: the pool's lock is not needed
+  for (int64_t j = 0; j < n_tokens; ++j) {
+    const int32_t pg = pages[j / ps];
+    if (pg < 0 || pg >= pool->n_pages)
+      return pool_fail(ASTR_ERR_INVALID, "astr_pool_slots: a page number is outside the pool");
+    slots[j] = (int32_t)((int64_t)pg * ps + j % ps);
+  }
+  return pool_ok();
+}
+
 }  // extern "C"

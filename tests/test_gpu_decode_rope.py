@@ -75,3 +75,35 @@ def test_fused_rejects_shapes_it_does_not_serve():
     with pytest.raises(A.AstrError) as e:
         _fused(dw)
     assert e.value.status == 2  # ASTR_ERR_UNSUPPORTED
+
+
+def test_fused_unsplit_plan_at_a_full_batch():
+    """Enough requests (batch x n_kv_heads >= 6 per SM) that the plan leaves every request
+    unsplit and launches no merge, the path of the mixed-batch step that bench.py times; lengths
+    cover one-token requests, page edges and several 128-token tiles."""
+    import torch
+    rng = np.random.default_rng(W.SEED_BASE + 870)
+    lens = rng.integers(1, 700, size=256)
+    lens[:6] = [1, 2, 15, 16, 17, 129]
+    seed = W.SEED_BASE + 871
+    mk = lambda: W.make_case("bf16", 16, 4, 128, 16, lens, None, with_rope=True, split_chunk=0,
+                             max_splits=16, seed=seed)
+    wl = mk()
+    two, one = DV.DeviceWorkload.upload(wl), DV.DeviceWorkload.upload(mk())
+    assert A.astr_decode_plan(one.decode["kv"], 16)[1] == 1
+    two.run_rope()
+    two.run_decode()
+    _fused(one)
+    torch.cuda.synchronize()
+    assert A.astr_device_error() == 0
+    assert np.array_equal(DV.to_host(one.k_buffer[1]), DV.to_host(two.k_buffer[1]))
+    assert np.array_equal(DV.to_host(one.v_buffer[1]), DV.to_host(two.v_buffer[1]))
+    assert np.array_equal(DV.to_host(one.decode["out"]), DV.to_host(two.decode["out"]))
+    r, d = wl.rope, wl.decode
+    kl = np.ascontiguousarray(wl.pool.k_buffer[1]).copy()
+    vl = np.ascontiguousarray(wl.pool.v_buffer[1]).copy()
+    q_ref = oracle.rope_kv_write(r.q, r.k, r.v, r.freqs_cis, r.position_ids, r.out_cache_loc, kl, vl)
+    assert np.array_equal(DV.to_host(one.k_buffer[1]), kl)
+    assert np.array_equal(DV.to_host(one.v_buffer[1]), vl)
+    ref = oracle.decode(q_ref, kl, vl, wl.pool.req_to_token, d.req_pool_indices, d.seq_lens)
+    assert np.max(np.abs(_f64(DV.to_host(one.decode["out"])) - ref)) <= 2e-2

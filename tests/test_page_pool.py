@@ -110,6 +110,11 @@ def test_argument_errors():
     with pytest.raises(A.AstrError):
         pool.page_info(4)
     assert list(pool.slots([3, 1], 6)) == [12, 13, 14, 15, 4, 5]
+    assert list(pool.slots([2], 0)) == []
+    with pytest.raises(A.AstrError):
+        pool.slots([3, 1], 9)  # two pages of 4 hold 8 tokens
+    with pytest.raises(A.AstrError):
+        pool.slots([3, 4], 6)  # page 4 is outside a 4-page pool
 
 
 def test_concurrent_threads_keep_the_pool_consistent():
