@@ -99,20 +99,74 @@ def read_peaks():
 
 
 class ClockSampler:
+    """SM clocks and clock-event reasons sampled during the timed region.
+
+    A host thread polls NVML (libnvidia-ml.so.1 through ctypes; read-only queries) every
+    `interval_s`, so that even a region of a few milliseconds holds several samples. Where NVML
+    cannot be loaded, `nvidia-smi -lms 100` runs instead."""
+
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReasons bits
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, interval_s: float = 0.001):
         self.idx = device_index
+        self.interval = interval_s
         self.proc = None
         self.path = None
         self.window = None  # host wall-clock bounds of the timed region
+        self.thread = None
+        self.rows = []
+        self.source = None
 
     def mark(self, t0: float, t1: float):
         self.window = (t0, t1)
 
+    def _nvml_handle(self):
+        import ctypes as C
+        nv = C.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = C.c_void_p()
+        try:  # the CUDA device's own GPU, whatever CUDA_VISIBLE_DEVICES maps it to
+            import torch
+            uid = "GPU-" + str(torch.cuda.get_device_properties(self.idx).uuid)
+            if nv.nvmlDeviceGetHandleByUUID(uid.encode(), C.byref(h)) == 0:
+                return nv, h
+        except Exception:
+            pass
+        if nv.nvmlDeviceGetHandleByIndex_v2(self.idx, C.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        return nv, h
+
+    def _poll(self, nv, h):
+        import ctypes as C
+        sm, smax, reasons = C.c_uint(), C.c_uint(), C.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, C.byref(smax))  # NVML_CLOCK_SM
+        while not self._stop:
+            t = time.time()
+            if nv.nvmlDeviceGetClockInfo(h, 1, C.byref(sm)) == 0 and \
+                    get_reasons(h, C.byref(reasons)) == 0:
+                names = [n for n, b in self.REASON_BITS.items() if reasons.value & b]
+                self.rows.append((t, float(sm.value), float(smax.value), names))
+            time.sleep(self.interval)
+
     def start(self):
+        self._stop = False
+        try:
+            import threading
+            nv, h = self._nvml_handle()
+            self.thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+            self.thread.start()
+            self.source = f"NVML every {self.interval * 1e3:g} ms"
+            return
+        except Exception:
+            self.thread = None
         try:
             fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
             os.close(fd)
@@ -121,19 +175,11 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi -lms 100"
         except Exception:
             self.proc = None
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.f.close()
+    def _read_smi(self):
         rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
@@ -148,6 +194,29 @@ class ClockSampler:
                 except ValueError:
                     continue
         os.unlink(self.path)
+        return rows
+
+    def stop(self):
+        if self.thread is not None:
+            time.sleep(0.01)
+            self._stop = True
+            self.thread.join(timeout=5)
+            rows = self.rows
+        elif self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+            rows = self._read_smi()
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        return self.summarize(rows)
+
+    def summarize(self, rows):
+        """rows: (host time, SM MHz, max SM MHz, [active reasons]) samples."""
         # only samples taken inside the timed region count; with none there (a region shorter
         # than the sampling interval), the nearest ones do and the record says so
         inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
@@ -155,10 +224,10 @@ class ClockSampler:
         sm = [r[1] for r in use]
         smax = [r[2] for r in use]
         reasons = set(n for r in use for n in r[3])
-        extra = {"samples": len(use), "in_timed_region": bool(inside)}
-        return dict({"sm_mhz": statistics.median(sm) if sm else None,
-                     "sm_max_mhz": max(smax) if smax else None,
-                     "reasons": sorted(reasons)}, **extra)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "in_timed_region": bool(inside), "source": self.source}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -491,9 +560,69 @@ def run_gpu(args):
         "gpu_launches": int(K * launches_per_step),
         "clocks": clk,
     }
+    if world == 1 and not args.no_configs:
+        out["configs"] = config_rows(args, peaks, local)
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(wl, 1.0, 1.0)
     print(json.dumps(out), flush=True)
+
+
+def config_rows(args, peaks, local):
+    """The other full-size configurations, one call each per step, timed on the GPU alone.
+
+    decode_b64_page1 (page-size-1 decode) and long_decode_b4 (fixed 4096-token split-K decode
+    with its merge) in GB/s of algorithmic bytes against the measured HBM copy bandwidth;
+    prefill_b8_varlen (varlen causal prefill, half the requests resumed) in TFLOP/s of unmasked
+    (query, key) pairs against the measured bf16 burst peak. Each of `args.steps` calls sits
+    between its own pair of CUDA events on the launching stream after `args.warmup` untimed
+    calls, and a 256 MB write flushes L2 before every call (outside the events)."""
+    import torch
+    from paged_kv_cache_apply_gb300 import device as DV
+    from paged_kv_cache_apply_gb300 import workloads as W
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name, op in (("decode_b64_page1", "decode"), ("prefill_b8_varlen", "prefill"),
+                     ("long_decode_b4", "decode")):
+        wl = W.make(name)
+        dw = DV.DeviceWorkload.upload(wl)
+        run = dw.run_decode if op == "decode" else dw.run_prefill
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        K = args.steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        clocks = ClockSampler(local)
+        clocks.start()
+        wall0 = time.time()
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        clocks.mark(wall0, time.time())
+        clk = clocks.stop()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        work = step_work(wl)
+        row = {"op": op, "ms": round(ms, 5), "workload": wl.description, "l2": "flushed before every call",
+               "clocks": clk}
+        if op == "decode":
+            gbs = work["decode_bytes"] / (ms * 1e-3) / 1e9
+            row.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                        "algorithmic_bytes": int(work["decode_bytes"]),
+                        "split_chunk": wl.decode.split_chunk})
+        else:
+            tfs = work["prefill_flops"] / (ms * 1e-3) / 1e12
+            row.update({"TFLOP/s": round(tfs, 2), "frac_tc": round(tfs / tc, 4),
+                        "algorithmic_flops": int(work["prefill_flops"])})
+        out[name] = row
+        del dw, wl
+        torch.cuda.empty_cache()
+    return out
 
 
 def _decode_source_sha():
@@ -553,6 +682,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the rows of the page-1 decode, varlen prefill and long decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -47,3 +47,19 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and np.isclose(cb["value"], line["value"])
     e = line["e2e"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0 and e["value"] == line["value"]
+
+
+def test_clock_summary_keeps_the_timed_region_only():
+    cs = bench.ClockSampler(0)
+    cs.source = "test"
+    cs.mark(10.0, 10.010)
+    rows = [(9.99, 1000.0, 2070.0, []), (10.001, 2070.0, 2070.0, []),
+            (10.004, 2055.0, 2070.0, ["sw_power_cap"]), (10.009, 2070.0, 2070.0, []),
+            (10.02, 900.0, 2070.0, ["hw_slowdown"])]
+    r = cs.summarize(rows)
+    assert r["in_timed_region"] and r["samples"] == 3
+    assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0
+    assert r["reasons"] == ["sw_power_cap"]
+    cs.mark(20.0, 20.001)  # no sample inside: all of them count, and the record says so
+    r = cs.summarize(rows)
+    assert not r["in_timed_region"] and r["samples"] == 5
