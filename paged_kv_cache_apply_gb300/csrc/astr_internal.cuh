@@ -168,6 +168,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
   }
 }
 
+// As mbar_wait, but each poll asks the hardware to suspend the thread for up to `hint_ns`
+// nanoseconds until the phase completes, so a waiting warp takes no issue slots from the
+// warps sharing its SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                                uint32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      raise_error(err, ASTR_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // 1-D bulk copy global -> shared, completion signalled on `bar` (bytes: multiple of 16,
 // both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,

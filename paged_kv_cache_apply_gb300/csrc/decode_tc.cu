@@ -802,10 +802,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int G>
+cudaError_t run_g(const DecArgs &a, const CUtensorMap &k16, const CUtensorMap &v16, int64_t grid,
+                  cudaStream_t s) {
+  auto k = decode_tc_kernel<G>;
+  static std::atomic<uint64_t> attr_devices{0};
+  cudaError_t e = raise_smem_limit_once(reinterpret_cast<const void *>(k), kSmemBytes, attr_devices);
+  if (e != cudaSuccess) return e;
+  if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, k16, v16);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 // Work counters: each launch takes the next of kSchedSlots pairs, so launches that overlap
 // on different streams use different ones unless kSchedSlots of them run at once. A launch's
-// last block puts its pair back to zero.
-__device__ unsigned g_dec_sched[2 * kSchedSlots];
+// last block puts its pair back to zero. The persistent decode and prefill kernels share them.
+__device__ unsigned g_sched[2 * kSchedSlots];
 constexpr int kMaxDevices = 64;
 std::mutex g_sched_mutex;
 unsigned *g_sched_ptr[kMaxDevices] = {};
@@ -821,7 +834,7 @@ cudaError_t sched_slot(unsigned **out, int *sms) {
     std::lock_guard<std::mutex> lock(g_sched_mutex);
     if (!g_sched_ptr[dev]) {
       void *p = nullptr;
-      if ((e = cudaGetSymbolAddress(&p, g_dec_sched)) != cudaSuccess) return e;
+      if ((e = cudaGetSymbolAddress(&p, g_sched)) != cudaSuccess) return e;
       if ((e = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
       g_sched_ptr[dev] = static_cast<unsigned *>(p);
@@ -832,18 +845,17 @@ cudaError_t sched_slot(unsigned **out, int *sms) {
   return cudaSuccess;
 }
 
-template <int G>
-cudaError_t run_g(const DecArgs &a, const CUtensorMap &k16, const CUtensorMap &v16, int64_t grid,
-                  cudaStream_t s) {
-  auto k = decode_tc_kernel<G>;
-  static std::atomic<uint64_t> attr_devices{0};
-  cudaError_t e = raise_smem_limit_once(reinterpret_cast<const void *>(k), kSmemBytes, attr_devices);
+cudaError_t device_sm_count(int *sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (grid > 0) k<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(a, k16, v16);
-  return cudaGetLastError();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_sched_mutex);
+  if (!g_sms[dev] && (e = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  *sms = g_sms[dev];
+  return cudaSuccess;
 }
-
-}  // namespace
 
 bool tc_decode_supported(int dtype, int head_dim, int group) {
   return dtype == ASTR_BF16 && head_dim == kD &&

@@ -64,12 +64,24 @@ cudaError_t launch_tc_prefill(const astr_kv_cache &kv, int32_t layer_id, const v
                               void *out, int32_t n_heads, uint64_t wait_ns, uint32_t *err,
                               cudaStream_t stream);
 
+// the persistent, pipelined form of the bf16 prefill (query groups of an even size); it is
+// launched when there are more (Q tile, head pair) items than SMs
+bool tc_prefill_pipe_supported(int group);
+cudaError_t launch_tc_prefill_pipe(const astr_kv_cache &kv, int32_t layer_id, const void *q, void *out,
+                                   int32_t n_heads, uint64_t wait_ns, uint32_t *err, cudaStream_t stream);
+
 // per-step metadata on the device (astr_bind_tasks); batch <= bind_tasks_max_batch()
 int bind_tasks_max_batch();
 cudaError_t launch_bind_tasks(const int32_t *q_lens, const int32_t *kv_lens, int32_t batch,
                               int32_t q_tile_rows, int32_t *qo_indptr, int32_t *kv_indptr,
                               int32_t *q_tile_to_batch, int32_t *q_tile_to_index,
                               int32_t max_tiles, int num_sms, uint32_t *err, cudaStream_t stream);
+
+// a pair of work counters on the current device for one launch of a persistent kernel
+// ([0]: claims, [1]: blocks done; the launch's last block zeroes both), and its SM count
+cudaError_t sched_slot(unsigned **out, int *sms);
+// the current device's SM count (looked up once per device)
+cudaError_t device_sm_count(int *sms);
 
 // sets the message astr_last_error() returns on this thread
 void set_last_error_message(const char *msg);

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+import paged_kv_cache_apply_gb300 as A
 from paged_kv_cache_apply_gb300 import build as B
 from paged_kv_cache_apply_gb300 import device as DV
 from paged_kv_cache_apply_gb300 import workloads as W
@@ -47,8 +48,13 @@ def test_decode_b64_page1():
 def test_prefill_b8_varlen_resumed():
     wl = W.prefill_b8_varlen()
     dw = DV.DeviceWorkload.upload(wl)
+    A.astr_device_error()  # clear
+    dw.prefill["out"].fill_(float("nan"))  # a row the kernel never writes stays NaN
     dw.run_prefill()
     _sync()
+    assert A.astr_device_error() == 0
+    import torch
+    assert not bool(torch.isnan(dw.prefill["out"]).any()), "prefill rows left unwritten"
     p = wl.prefill
     rng = np.random.default_rng(3)
     rows = set()

@@ -147,6 +147,12 @@ PREFILL_CASES = [
     ("bf16", 32, 4, 128, 16, [600, 129], [256, 129]),      # G = 8: four head pairs per group
     ("bf16", 16, 4, 128, 1, [400, 129, 64], [400, 1, 64]),  # page 1: no page runs, all cp.async
     ("bf16", 16, 4, 128, 16, [50, 500, 20], [0, 300, 20]),  # a request with no new rows
+    # 400 head-pair items for at most 152 blocks: every block of the persistent kernel runs
+    # several items in turn (whole tiles, tiles cut by the request's end, resumed prefixes)
+    ("bf16", 4, 2, 128, 16, [129 + 37 * (b % 5) for b in range(100)], [129 - (b % 3) * 60 for b in range(100)]),
+    # 232 items with G = 4 on one-token pages: every K/V row comes by cp.async, with prefixes
+    ("bf16", 16, 4, 128, 1, [129, 300, 256, 400, 140, 260, 535, 129, 257, 190, 300, 480],
+     [129, 200, 256, 300, 140, 260, 135, 129, 257, 190, 300, 280]),
 ]
 
 
@@ -161,6 +167,7 @@ def test_prefill_cases(dtype, H, Hk, D, page, kv_lens, q_lens):
     ref = oracle.prefill(p.q, kl, vl, wl.pool.req_to_token, p.req_pool_indices, p.qo_indptr,
                          p.kv_indptr)
     assert maxerr(DV.to_host(dw.prefill["out"]), ref) <= TOL[dtype]
+    assert A.astr_device_error() == 0  # no bounded wait ran out, no index was rejected
 
 
 @pytest.mark.parametrize("dtype,D,G,page", [("bf16", 128, 4, 16), ("f32", 64, 2, 1),
