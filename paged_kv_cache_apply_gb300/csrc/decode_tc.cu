@@ -701,24 +701,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) *abort_flag = 1;
   } else {
-    // ================================ MMA issuer (one lane) ===================================
-    if (lane == 0) {
+    // ============ MMA issuer: warp 8, converged; one elected lane issues each MMA ============
+    // Descriptors are built once per buffer and stepped by constants (16-byte units): an MMA
+    // loop run by one lane with two descriptors built per MMA measured about 120 cycles an
+    // issue, most of a tile's time on one-token pages.
+    {
+      auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const bool got = !*abort_flag && mbar_wait(bar, parity, a.wait_ns, a.err);
+        return __all_sync(0xffffffffu, got);
+      };
+      const uint64_t k_desc = tc::desc_sw128(sbase + kOffK, 16, 1024);           // K stage 0 (A of S^T)
+      const uint64_t q_desc = tc::desc_sw128(sbase + kOffQ, 16, 1024);           // Q buffer 0 (B of S^T)
+      const uint64_t v_desc = tc::desc_sw128(sbase + kOffV, kBlockBytes, 1024);  // V stage 0, MN-major
+      const uint64_t p_desc = tc::desc_sw128(sbase + kOffP, 16, 1024);           // P^T buffer 0 (B)
+      constexpr uint64_t kStageStep = kTileBytes >> 4, kBufStep = 4096 >> 4;
       // O^T += V^T P^T for tile i (P^T from buffer i & 1) into O buffer ob; `first` starts it
       auto pv = [&](uint32_t i, int ob, bool first) -> bool {
         const int sb = i & 1, st = i % kStages;
-        if (!mbar_wait(&p_full[sb], (i >> 1) & 1, a.wait_ns, a.err)) return false;
+        if (!wait(&p_full[sb], (i >> 1) & 1)) return false;
         tc::fence_after_sync();
         tc::fence_proxy_async_smem();
-        const uint32_t vaddr = sbase + kOffV + st * kTileBytes;
-        const uint32_t paddr = sbase + kOffP + sb * 4096;
+        const uint64_t vd = v_desc + (uint64_t)st * kStageStep, pd = p_desc + (uint64_t)sb * kBufStep;
 #pragma unroll
-        for (int ks = 0; ks < kTok / 16; ++ks) {
-          const uint64_t ad = tc::desc_sw128(vaddr + ks * 2048, kBlockBytes, 1024);
-          const uint64_t bd = tc::desc_sw128(paddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
-          tc::mma_ss(tO0 + ob * 16, ad, bd, kIdescPV, (!first || ks > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(&empty[st]);
-        tc::mma_commit(&pv_done[sb]);
+        for (int ks = 0; ks < kTok / 16; ++ks)
+          tc::mma_ss_elect(tO0 + ob * 16, vd + (uint64_t)ks * (2048 >> 4),
+                           pd + (uint64_t)((ks >> 2) * (2048 >> 4) + (ks & 3) * 2), kIdescPV,
+                           (!first || ks > 0) ? 1u : 0u);
+        tc::mma_commit_elect(&empty[st]);
+        tc::mma_commit_elect(&pv_done[sb]);
         return true;
       };
       bool ok = true;
@@ -728,41 +738,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool prev_first = false;
       for (uint32_t n = 0; ok; ++n) {
         DecItem w;
-        if (!take(n, w)) {
+        if (!wait(&item_full[n & 1], (n >> 1) & 1)) {
           ok = false;
           break;
         }
+        w = ring[n & 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&item_empty[n & 1]);
         if (w.ntiles == 0) break;
         const int qb = n & 1, ob = n & 1;
-        if (!mbar_wait(&q_full[qb], (n >> 1) & 1, a.wait_ns, a.err)) {
+        if (!wait(&q_full[qb], (n >> 1) & 1)) {
           ok = false;
           break;
         }
-        const uint32_t qaddr = sbase + kOffQ + qb * 4096;
+        const uint64_t qd = q_desc + (uint64_t)qb * kBufStep;
         for (int j = 0; j < w.ntiles && ok; ++j, ++it) {
           const int st = it % kStages, sb = it & 1;
-          if (*abort_flag || !mbar_wait(&full[st], (it / kStages) & 1, a.wait_ns, a.err)) {
+          if (!wait(&full[st], (it / kStages) & 1)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
           tc::fence_proxy_async_smem();
-          const uint32_t kaddr = sbase + kOffK + st * kTileBytes;
+          const uint64_t kd = k_desc + (uint64_t)st * kStageStep;
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint64_t ad = tc::desc_sw128(kaddr + (ks >> 2) * kBlockBytes + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = tc::desc_sw128(qaddr + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024);
-            tc::mma_ss(tS0 + sb * 16, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(&s_full[sb]);
-          if (j + 1 == w.ntiles) tc::mma_commit(&q_empty[qb]);  // the item's last read of Q
+          for (int ks = 0; ks < kD / 16; ++ks)
+            tc::mma_ss_elect(tS0 + sb * 16, kd + (uint64_t)((ks >> 2) * (kBlockBytes >> 4) + (ks & 3) * 2),
+                             qd + (uint64_t)((ks >> 2) * (2048 >> 4) + (ks & 3) * 2), kIdescQK, ks > 0 ? 1u : 0u);
+          tc::mma_commit_elect(&s_full[sb]);
+          if (j + 1 == w.ntiles) tc::mma_commit_elect(&q_empty[qb]);  // the item's last read of Q
           if (have_prev && !pv(it - 1, prev_ob, prev_first)) {
             ok = false;
             break;
           }
           // this tile's P.V goes in after the next tile's S; the first one of an item waits for
           // the epilogue of the item two back to have read the O buffer
-          if (j == 0 && n >= 2 && !mbar_wait(&o_free[ob], ((n >> 1) - 1) & 1, a.wait_ns, a.err)) {
+          if (j == 0 && n >= 2 && !wait(&o_free[ob], ((n >> 1) - 1) & 1)) {
             ok = false;
             break;
           }
@@ -779,10 +790,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && have_prev && !pv(it - 1, prev_ob, prev_first)) ok = false;
       if (!ok) *abort_flag = 1;
-      tc::mma_commit(drain);  // nothing may still be in flight when TMEM is freed
+      tc::mma_commit_elect(drain);  // nothing may still be in flight when TMEM is freed
       mbar_wait(drain, 0, kDrainLimitNs, a.err);
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   tc::fence_before_sync();
