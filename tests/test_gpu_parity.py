@@ -153,6 +153,8 @@ PREFILL_CASES = [
     # 232 items with G = 4 on one-token pages: every K/V row comes by cp.async, with prefixes
     ("bf16", 16, 4, 128, 1, [129, 300, 256, 400, 140, 260, 535, 129, 257, 190, 300, 480],
      [129, 200, 256, 300, 140, 260, 135, 129, 257, 190, 300, 280]),
+    # G = 8 with more items than SMs: four head pairs per KV group in the persistent kernel
+    ("bf16", 32, 4, 128, 16, [300, 256, 400, 512, 256, 384], [256, 256, 256, 300, 256, 384]),
 ]
 
 
