@@ -546,17 +546,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_2d(vst + hf * kBlockBytes + t0 * 128, &v16, w.g * kD + hf * 64, y, &full[st]);
             }
           }
-        } else
-#pragma unroll 4
-        for (int jj = 0; jj < 16; ++jj) {
-          const int tl = jj * 2 + half;         // token within this warp's 32
-          const int t = lw * 32 + tl;           // token within the tile
-          const int64_t s = __shfl_sync(0xffffffffu, my, tl);
-          const uint32_t off = tc::sw128_chunk_offset(t, c, kBlockBytes);
-          const bool v = s >= 0;
-          const int64_t go = v ? s * rowb + c * 16 : 0;
-          tc::cp_async16(kst + off, kg + go, v ? 16u : 0u);
-          tc::cp_async16(vst + off, vg + go, v ? 16u : 0u);
+        } else {
+          // the slots of the 16 token rows this lane copies a chunk of (checked above to lie in
+          // [0, size) or be -1; they come from int32 page-table entries), all gathered before
+          // any copy so the 32 copies issue back to back
+          int32_t sl[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) sl[jj] = __shfl_sync(0xffffffffu, (int32_t)my, jj * 2 + half);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int t = lw * 32 + jj * 2 + half;  // token within the tile
+            const uint32_t off = tc::sw128_chunk_offset(t, c, kBlockBytes);
+            const bool v = sl[jj] >= 0;
+            const int64_t go = v ? (int64_t)sl[jj] * rowb + c * 16 : 0;
+            tc::cp_async16(kst + off, kg + go, v ? 16u : 0u);
+            tc::cp_async16(vst + off, vg + go, v ? 16u : 0u);
+          }
         }
         tc::cp_async_arrive_noinc(&full[st]);
       }
