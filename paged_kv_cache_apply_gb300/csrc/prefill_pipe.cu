@@ -62,6 +62,10 @@ constexpr int kOffP = kOffQ + 2 * kTile;          // P_0, P_1 (also the output s
 constexpr int kOffKV = kOffP + 2 * kTile;         // K/V ring
 constexpr int kOffBar = kOffKV + kRing * kTile;
 constexpr int kNumBars = 32;
+// barrier indices in the array at kOffBar (each 8 bytes)
+constexpr int kBarItemFull = 0, kBarItemEmpty = 2, kBarQFull = 4, kBarQEmpty = 5, kBarKvFull = 6,
+              kBarKvEmpty = 9, kBarSFull = 12, kBarSFree = 14, kBarPFull = 16, kBarPFree = 18,
+              kBarOFree = 22, kBarStageFull = 24, kBarStageFree = 26, kBarDrain = 28;
 constexpr int kOffItem = kOffBar + kNumBars * 8;  // two published items
 constexpr int kOffMisc = kOffItem + 2 * 64;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;  // + alignment slack
@@ -117,20 +121,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-  uint64_t *item_full = bars + 0;    // [2] scheduler -> all roles (1 arrival)
-  uint64_t *item_empty = bars + 2;   // [2] 8 softmax warps, loader warp 10, 2 MMA threads
-  uint64_t *q_full = bars + 4;       // TMA (transaction bytes)
-  uint64_t *q_empty = bars + 5;      // one arrival per head once the item's last S has completed
-  uint64_t *kv_full = bars + 6;      // [3] per loader warp: 32 lanes (cp.async) + one expect-tx
-  uint64_t *kv_empty = bars + 9;     // [3] one arrival per head once its MMAs on the tile completed
-  uint64_t *s_full = bars + 12;      // [2] per head, MMA commit
-  uint64_t *s_free = bars + 14;      // [2] per head, 128 arrivals (scores read out of TMEM)
-  uint64_t *p_full = bars + 16;      // [2] per head, 128 arrivals (P in shared memory)
-  uint64_t *p_free = bars + 18;      // [2] per head, MMA commit after P.V
-  uint64_t *o_free = bars + 22;      // [2] per head, 128 arrivals (O read out of TMEM)
-  uint64_t *stage_full = bars + 24;  // [2] per head, 128 arrivals (output tile staged)
-  uint64_t *stage_free = bars + 26;  // [2] per head, 1 arrival (the TMA store has read it)
-  uint64_t *drain = bars + 28;       // [2] per MMA thread
+  uint64_t *item_full = bars + kBarItemFull;    // [2] scheduler -> all roles (1 arrival)
+  uint64_t *item_empty = bars + kBarItemEmpty;  // [2] 8 softmax warps, loader warp 10, 2 MMA threads
+  uint64_t *q_full = bars + kBarQFull;          // TMA (transaction bytes)
+  uint64_t *q_empty = bars + kBarQEmpty;        // one arrival per head once the item's last S has completed
+  uint64_t *kv_full = bars + kBarKvFull;        // [3] per loader warp: 32 lanes (cp.async) + one expect-tx
+  uint64_t *kv_empty = bars + kBarKvEmpty;      // [3] one arrival per head once its MMAs on the tile completed
+  uint64_t *s_full = bars + kBarSFull;          // [2] per head, MMA commit
+  uint64_t *s_free = bars + kBarSFree;          // [2] per head, 128 arrivals (scores read out of TMEM)
+  uint64_t *p_full = bars + kBarPFull;          // [2] per head, 128 arrivals (P in shared memory)
+  uint64_t *p_free = bars + kBarPFree;          // [2] per head, MMA commit after P.V
+  uint64_t *o_free = bars + kBarOFree;          // [2] per head, 128 arrivals (O read out of TMEM)
+  uint64_t *stage_full = bars + kBarStageFull;  // [2] per head, 128 arrivals (output tile staged)
+  uint64_t *stage_free = bars + kBarStageFree;  // [2] per head, 1 arrival (the TMA store has read it)
+  uint64_t *drain = bars + kBarDrain;           // [2] per MMA thread
   PipeItem *items = reinterpret_cast<PipeItem *>(smem + kOffItem);
   // per ring slot: c + 1 when fill c of the slot holds rows written by cp.async (generic
   // proxy), which the tensor core may read only after a proxy fence
@@ -183,55 +187,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + h * 128 + lane_base;
     const uint32_t tO = tmem + 256 + h * 128 + lane_base;
     const uint32_t poff = kOffP + h * kTile;
+    // The softmax addresses its barriers and its P tile through 32-bit shared-window addresses:
+    // one base register plus constants, which leaves more registers to the 128 scores of a row.
+    const uint32_t sbar = sbase + kOffBar;
+    auto bar = [&](int i) -> uint32_t { return sbar + 8u * (uint32_t)i; };
+    // this row's 128-byte line of the P tile with the row's swizzle in the chunk bits; the tile is
+    // 1024-byte aligned, so chunk c of the row is at (prow ^ (c % 8) * 16) + (c / 8) * kBlk
+    const uint32_t prow = sbase + poff + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u +
+                          ((uint32_t)(r & 7) << 4);
     uint32_t n = 0, T = 0, ns = 0;  // items, tiles, staged stores
     uint32_t cs = 0;                // K/V ring fills before the current item
     bool staged = false;            // a TMA store may still be reading the P buffer
     // a ring slot or the Q buffer is free once both heads' MMAs on it have completed: the
     // first thread of each head arrives when it sees that completion
-    auto release = [&](uint64_t *bar) {
-      if (r == 0) mbar_arrive(bar);
+    auto release = [&](uint32_t b) {
+      if (r == 0) mbar_arrive(b);
     };
     bool aborted = false;
     // a wait whose outcome is the same for the whole warp (the TMEM loads and stores that
     // follow are warp-collective)
-    auto wait_warp = [&](uint64_t *bar, uint32_t parity) -> bool {
-      const bool got = mbar_wait_sleep(bar, parity, a.wait_ns, a.err);
+    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool got = mbar_wait_sleep(b, parity, a.wait_ns, a.err);
       return __all_sync(0xffffffffu, got);
     };
     while (!aborted) {
-      if (!wait_warp(&item_full[n & 1], (n >> 1) & 1)) {
+      if (!wait_warp(bar(kBarItemFull + (n & 1)), (n >> 1) & 1)) {
         aborted = true;
         break;
       }
       const PipeItem it = items[n & 1];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&item_empty[n & 1]);
+      if (lane == 0) mbar_arrive(bar(kBarItemEmpty + (n & 1)));
       if (it.nkv == 0) break;
-      const int64_t pos = it.Pb + it.r0 + r;  // absolute position of this row
-      const int64_t pos_min = it.Pb + it.r0;
-      const int64_t lim_row = (pos + 1 < it.Kb ? pos + 1 : it.Kb);  // keys [0, lim_row) visible
+      // keys [0, lim_row) are visible to this row; the tiles from j_mask on need masking (the
+      // first tile that crosses the diagonal or the end of the request, and all after it)
+      const int32_t lim_row = (int32_t)(it.Pb + it.r0 + r + 1 < it.Kb ? it.Pb + it.r0 + r + 1 : it.Kb);
+      const int64_t j_diag = it.Pb + it.r0 >= kKeys - 1 ? (it.Pb + it.r0 - (kKeys - 1)) / kKeys + 1 : 0;
+      const int64_t j_end = it.Kb >= kKeys ? (it.Kb - kKeys) / kKeys + 1 : 0;
+      const int32_t j_mask = (int32_t)(j_diag < j_end ? j_diag : j_end);
       float m = -INFINITY, l = 0.f;
       // the ring carries K0, K1, V0, K2, V1, ..., V_{nkv-1}: K_j is fill cs + 2j - 1 (K_0: cs),
       // V_j is fill cs + 2j + 2 (the last V: cs + 2 nkv - 1)
       for (int j = 0; j < it.nkv; ++j, ++T) {
-        if (!wait_warp(&s_full[h], T & 1)) {
+        if (!wait_warp(bar(kBarSFull + h), T & 1)) {
           aborted = true;
           break;
         }
         tc::fence_after_sync();
-        release(&kv_empty[(cs + (j == 0 ? 0 : 2 * j - 1)) % kRing]);
-        if (j + 1 == it.nkv) release(q_empty);
+        release(bar(kBarKvEmpty + ((cs + (j == 0 ? 0 : 2 * j - 1))) % kRing));
+        if (j + 1 == it.nkv) release(bar(kBarQEmpty));
         uint32_t sv[128];
-        tc::tmem_ld32(tS, sv);
-        tc::tmem_ld32(tS + 32, sv + 32);
-        tc::tmem_ld32(tS + 64, sv + 64);
-        tc::tmem_ld32(tS + 96, sv + 96);
+        tc::tmem_ld128(tS, sv);
         tc::tmem_ld_wait();
         tc::fence_before_sync();
-        mbar_arrive(&s_free[h]);  // the tensor core may write the next S here now
-        if ((int64_t)j * kKeys + kKeys - 1 > pos_min || (int64_t)j * kKeys + kKeys > it.Kb) {
-          const int64_t lim = lim_row - (int64_t)j * kKeys;
-          const int nvalid = lim < 0 ? 0 : (lim > kKeys ? kKeys : (int)lim);
+        mbar_arrive(bar(kBarSFree + h));  // the tensor core may write the next S here now
+        if (j >= j_mask) {
+          const int32_t lim = lim_row - j * kKeys;
+          const int nvalid = lim < 0 ? 0 : (lim > kKeys ? kKeys : lim);
 #pragma unroll
           for (int k = 0; k < kKeys; ++k) sv[k] = k < nvalid ? sv[k] : 0xFF800000u;  // -inf
         }
@@ -252,18 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the P buffer is free (and O settled) once the previous P.V has completed; for an
         // item's first tile, once the last output staged in the buffer has been read
         if (j > 0) {
-          if (!wait_warp(&p_free[h], (T - 1) & 1)) {
+          if (!wait_warp(bar(kBarPFree + h), (T - 1) & 1)) {
             aborted = true;
             break;
           }
           tc::fence_after_sync();
-          release(&kv_empty[(cs + 2 * j) % kRing]);  // V_{j-1}
+          release(bar(kBarKvEmpty + ((cs + 2 * j)) % kRing));  // V_{j-1}
         } else if (staged) {
           if (r == 0) {
             tc::bulk_wait_read_all();
-            mbar_arrive(&stage_free[h]);
+            mbar_arrive(bar(kBarStageFree + h));
           }
-          if (!wait_warp(&stage_free[h], (ns - 1) & 1)) {
+          if (!wait_warp(bar(kBarStageFree + h), (ns - 1) & 1)) {
             aborted = true;
             break;
           }
@@ -285,8 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sum2[k >> 1] = fadd2(sum2[k >> 1], make_float2(p0, p1));
             pk[k >> 1] = pack_bf16x2_rn(p0, p1);
           }
-          *reinterpret_cast<uint4 *>(smem + poff + tc::sw128_chunk_offset(r, c, kBlk)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          st_shared_v4((prow ^ (uint32_t)((c & 7) << 4)) + (uint32_t)(c >> 3) * kBlk, pk[0], pk[1], pk[2], pk[3]);
         }
         const float2 s01 = fadd2(sum2[0], sum2[1]), s23 = fadd2(sum2[2], sum2[3]);
         l += (s01.x + s01.y) + (s23.x + s23.y);
@@ -305,18 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
         tc::fence_before_sync();
-        mbar_arrive(&p_full[h]);
+        mbar_arrive(bar(kBarPFull + h));
       }
       if (aborted) break;
       // ---- epilogue: O / l to bf16; whole tiles through the P buffer as two TMA boxes, a tile
       // cut by the request's end row by row (a box would overwrite the next request's rows)
       // O is complete with the item's last P.V
-      if (!wait_warp(&p_free[h], (T - 1) & 1)) {
+      if (!wait_warp(bar(kBarPFree + h), (T - 1) & 1)) {
         aborted = true;
         break;
       }
       tc::fence_after_sync();
-      release(&kv_empty[(cs + 2 * it.nkv - 1) % kRing]);  // V_last
+      release(bar(kBarKvEmpty + ((cs + 2 * it.nkv - 1)) % kRing));  // V_last
       cs += 2 * it.nkv;
       const bool by_tma = a.tma_out && it.rows_here == kRows;  // uniform over the head
       const float inv = 1.f / l;
@@ -341,12 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc::fence_before_sync();
-      mbar_arrive(&o_free[h]);  // the next item's first P.V may overwrite O
+      mbar_arrive(bar(kBarOFree + h));  // the next item's first P.V may overwrite O
       if (by_tma) {
         tc::fence_proxy_async_smem();
-        mbar_arrive(&stage_full[h]);
+        mbar_arrive(bar(kBarStageFull + h));
         if (r == 0) {
-          if (mbar_wait_sleep(&stage_full[h], ns & 1, a.wait_ns, a.err)) {
+          if (mbar_wait_sleep(bar(kBarStageFull + h), ns & 1, a.wait_ns, a.err)) {
             tc::tma_store_2d(&omap, (it.h0 + h) * kD, (int)(it.q0 + it.r0), sbase + poff);
             tc::tma_store_2d(&omap, (it.h0 + h) * kD + 64, (int)(it.q0 + it.r0), sbase + poff + kBlk);
             tc::bulk_commit();
