@@ -40,6 +40,22 @@ struct Chunk;
 
 template <>
 struct Chunk<float> {
+  struct Raw {
+    float4 a, b;
+  };
+  static __device__ __forceinline__ Raw load_raw(const void *base, int64_t off) {
+    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + off);
+    return Raw{__ldg(p), __ldg(p + 1)};
+  }
+  static __device__ __forceinline__ void unpack(const Raw &w, float (&x)[8]) {
+    x[0] = w.a.x; x[1] = w.a.y; x[2] = w.a.z; x[3] = w.a.w;
+    x[4] = w.b.x; x[5] = w.b.y; x[6] = w.b.z; x[7] = w.b.w;
+  }
+  static __device__ __forceinline__ void store_raw(void *base, int64_t off, const Raw &w) {
+    float4 *p = reinterpret_cast<float4 *>(static_cast<float *>(base) + off);
+    p[0] = w.a;
+    p[1] = w.b;
+  }
   static __device__ __forceinline__ void load(const void *base, int64_t off, float (&x)[8]) {
     const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + off);
     float4 a = __ldg(p), b = __ldg(p + 1);
@@ -61,6 +77,17 @@ struct Chunk<float> {
 
 template <>
 struct Chunk<bf16_t> {
+  using Raw = uint4;
+  static __device__ __forceinline__ Raw load_raw(const void *base, int64_t off) {
+    return __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + off));
+  }
+  static __device__ __forceinline__ void unpack(const Raw &w, float (&x)[8]) {
+    x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
+    x[4] = bf16_lo(w.z); x[5] = bf16_hi(w.z); x[6] = bf16_lo(w.w); x[7] = bf16_hi(w.w);
+  }
+  static __device__ __forceinline__ void store_raw(void *base, int64_t off, const Raw &w) {
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + off) = w;
+  }
   static __device__ __forceinline__ void load(const void *base, int64_t off, float (&x)[8]) {
     uint4 w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + off));
     x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
@@ -176,6 +203,81 @@ __global__ void __launch_bounds__(512) rope_kv_write_token_kernel(const RopeArgs
       Chunk<T>::store(a.k_layer, ((int64_t)s * a.Hk + g) * a.D + e0, y);
     }
   }
+}
+
+// One block of kTokThreads threads per token; thread i takes the token's chunks i, i + kTokThreads,
+// ... (NC of them). A thread issues all its row loads before it reads the position and the slot,
+// so they are in flight together with those two loads; only the (cos, sin) loads wait for the
+// position and only the stores for the slot. Small blocks let every token of a step be resident
+// at once, which keeps enough bytes in flight on every SM.
+constexpr int kTokThreads = 128;
+
+template <typename T, int NC>
+__global__ void __launch_bounds__(kTokThreads) rope_kv_write_token_nc_kernel(const RopeArgs a) {
+  const int64_t t = blockIdx.x;
+  const int chunk_shift = a.D == 128 ? 4 : 3;
+  const int per_token = (a.H + 2 * a.Hk) << chunk_shift;
+  const int32_t p = __ldg(a.pos + t);
+  const int32_t s = __ldg(a.loc + t);
+  typename Chunk<T>::Raw raw[NC];
+#pragma unroll
+  for (int k = 0; k < NC; ++k) {
+    const int c = threadIdx.x + k * kTokThreads;
+    if (c < per_token) {
+      const int row = c >> chunk_shift;
+      const int e0 = (c - (row << chunk_shift)) << 3;
+      if (row < a.H)
+        raw[k] = Chunk<T>::load_raw(a.q, (t * a.H + row) * a.D + e0);
+      else if (row < a.H + a.Hk)
+        raw[k] = Chunk<T>::load_raw(a.k, (t * a.Hk + (row - a.H)) * a.D + e0);
+      else
+        raw[k] = Chunk<T>::load_raw(a.v, (t * a.Hk + (row - a.H - a.Hk)) * a.D + e0);
+    }
+  }
+  const bool pos_ok = p >= 0 && p < a.freqs_max_len;
+  const bool slot_ok = s >= 0 && (int64_t)s < a.size;
+  if (!(pos_ok && slot_ok)) {
+    if (threadIdx.x == 0) raise_error(a.err, (pos_ok ? 0u : ASTR_DEVERR_POS) | (slot_ok ? 0u : ASTR_DEVERR_SLOT));
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < NC; ++k) {
+    const int c = threadIdx.x + k * kTokThreads;
+    if (c < per_token) {
+      const int row = c >> chunk_shift;
+      const int e0 = (c - (row << chunk_shift)) << 3;
+      if (row >= a.H + a.Hk) {  // value head: copied unchanged
+        Chunk<T>::store_raw(a.v_layer, ((int64_t)s * a.Hk + (row - a.H - a.Hk)) * a.D + e0, raw[k]);
+        continue;
+      }
+      float cs[8];
+      {
+        const float4 *f = reinterpret_cast<const float4 *>(a.freqs + (int64_t)p * a.D + 2 * (e0 >> 1));
+        float4 f0 = __ldg(f), f1 = __ldg(f + 1);
+        cs[0] = f0.x; cs[1] = f0.y; cs[2] = f0.z; cs[3] = f0.w;
+        cs[4] = f1.x; cs[5] = f1.y; cs[6] = f1.z; cs[7] = f1.w;
+      }
+      float x[8], y[8];
+      Chunk<T>::unpack(raw[k], x);
+      rotate4(x, cs, y);
+      if (row < a.H)
+        Chunk<T>::store(a.q_out, (t * a.H + row) * a.D + e0, y);
+      else
+        Chunk<T>::store(a.k_layer, ((int64_t)s * a.Hk + (row - a.H)) * a.D + e0, y);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_token_nc(const RopeArgs &a, int nc, unsigned blocks, cudaStream_t stream) {
+  switch (nc) {
+    case 1: rope_kv_write_token_nc_kernel<T, 1><<<blocks, kTokThreads, 0, stream>>>(a); break;
+    case 2: rope_kv_write_token_nc_kernel<T, 2><<<blocks, kTokThreads, 0, stream>>>(a); break;
+    case 3: rope_kv_write_token_nc_kernel<T, 3><<<blocks, kTokThreads, 0, stream>>>(a); break;
+    case 4: rope_kv_write_token_nc_kernel<T, 4><<<blocks, kTokThreads, 0, stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 // RoPE with no cache write (the training path): q_out = R q and k_out = R k, or with Inverse
@@ -306,6 +408,11 @@ cudaError_t launch_rope_kv_write(const astr_kv_cache &kv, int32_t layer_id, cons
   if (total == 0) return cudaSuccess;
   if (kv.n_tokens <= INT32_MAX) {  // a block per token
     const int64_t per_token = (int64_t)(n_heads + 2 * kv.n_kv_heads) * (kv.head_dim / 8);
+    const int nc = (int)((per_token + kTokThreads - 1) / kTokThreads);
+    if (nc <= 4) {
+      if (kv.dtype == ASTR_BF16) return launch_token_nc<bf16_t>(a, nc, (unsigned)kv.n_tokens, stream);
+      return launch_token_nc<float>(a, nc, (unsigned)kv.n_tokens, stream);
+    }
     const int threads = per_token >= 512 ? 512 : (int)((per_token + 31) / 32 * 32);
     if (kv.dtype == ASTR_BF16)
       rope_kv_write_token_kernel<bf16_t><<<(unsigned)kv.n_tokens, threads, 0, stream>>>(a);
