@@ -390,6 +390,12 @@ def run_gpu(args):
     pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
     serial_ms = statistics.mean(e[0].elapsed_time(e[3]) for e in ev)
+    # the same ops' marginal costs in a stream (no event between kernels; L2 flushed before each)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    rope_mg = marginal_ms(dw.run_rope, flush, stream, K)
+    pre_mg = marginal_ms(dw.run_prefill, flush, stream, K)
+    dec_mg = marginal_ms(dw.run_decode, flush, stream, min(K, 20))
+    del flush
 
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -493,6 +499,9 @@ def run_gpu(args):
     dec_gbs = work["decode_bytes"] / (dec_ms * 1e-3) / 1e9
     rope_gbs = work["rope_bytes"] / (rope_ms * 1e-3) / 1e9
     pre_tflops = work["prefill_flops"] / (pre_ms * 1e-3) / 1e12
+    rope_gbs_mg = work["rope_bytes"] / (rope_mg * 1e-3) / 1e9
+    pre_tflops_mg = work["prefill_flops"] / (pre_mg * 1e-3) / 1e12
+    dec_gbs_mg = work["decode_bytes"] / (dec_mg * 1e-3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if os.path.exists(tpath):
@@ -530,17 +539,26 @@ def run_gpu(args):
                        "main stream, concurrently: the decode with the rope + write of its 256 "
                        "new tokens folded in (astr_decode_attention_rope); the step ends when "
                        "both are done",
-            "timing": "rows and roofline: K steps with the ops serialised and an event between "
-                      "them; then value: K steps with CUDA events at the ends only",
+            "timing": "rows: each op's marginal cost in a stream (K pairs of a 256 MB L2 flush "
+                      "and the op between two events, minus K flushes; median of 3), with the "
+                      "time between an event on each side of the op as ms_between_events; "
+                      "roofline: K steps with the ops serialised and an event between them; "
+                      "value: K steps with CUDA events at the ends only",
             "decode_split_chunk": chunk, "decode_splits": n_splits,
         },
         "rows": {
-            "rope_kv_write": {"ms": round(rope_ms, 5), "GB/s": round(rope_gbs, 1),
-                              "frac_hbm": round(rope_gbs / hbm, 4)},
-            "prefill": {"ms": round(pre_ms, 5), "TFLOP/s": round(pre_tflops, 2),
-                        "frac_tc": round(pre_tflops / tc, 4)},
-            "decode": {"ms": round(dec_ms, 5), "GB/s": round(dec_gbs, 1),
-                       "frac_hbm": round(dec_gbs / hbm, 4)},
+            "rope_kv_write": {"ms": round(rope_mg, 5), "GB/s": round(rope_gbs_mg, 1),
+                              "frac_hbm": round(rope_gbs_mg / hbm, 4),
+                              "ms_between_events": round(rope_ms, 5),
+                              "frac_hbm_between_events": round(rope_gbs / hbm, 4)},
+            "prefill": {"ms": round(pre_mg, 5), "TFLOP/s": round(pre_tflops_mg, 2),
+                        "frac_tc": round(pre_tflops_mg / tc, 4),
+                        "ms_between_events": round(pre_ms, 5),
+                        "frac_tc_between_events": round(pre_tflops / tc, 4)},
+            "decode": {"ms": round(dec_mg, 5), "GB/s": round(dec_gbs_mg, 1),
+                       "frac_hbm": round(dec_gbs_mg / hbm, 4),
+                       "ms_between_events": round(dec_ms, 5),
+                       "frac_hbm_between_events": round(dec_gbs / hbm, 4)},
             "serialised_step": {"ms": round(serial_ms, 5)},
         },
         "roofline": {"kernel": ("astr_decode_attention call: decode_tc_kernel partials + "
@@ -567,6 +585,34 @@ def run_gpu(args):
     print(json.dumps(out), flush=True)
 
 
+def marginal_ms(fn, flush, stream, K, rounds=3):
+    """The cost of one call of `fn` in a stream of launches: K pairs (an L2 flush, then `fn`)
+    between two CUDA events, minus K flushes alone, the median over `rounds` alternations.
+
+    A short kernel timed between its own pair of events also carries the events' cost: on GB300
+    an event on each side of a trivial kernel measures 4.4-6 us, most of a 10 us op. Here the
+    launches follow one another with no event between them, as in a model's step, and the flush
+    (a 256 MB write, larger than the 129 MB L2) makes every call read its inputs from HBM."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(with_fn):
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            if with_fn:
+                fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    diffs = []
+    for _ in range(rounds):
+        diffs.append(timed(True) - timed(False))
+    return statistics.median(diffs)
+
+
 def config_rows(args, peaks, local):
     """The other full-size configurations, one call each per step, timed on the GPU alone.
 
@@ -575,7 +621,8 @@ def config_rows(args, peaks, local):
     prefill_b8_varlen (varlen causal prefill, half the requests resumed) in TFLOP/s of unmasked
     (query, key) pairs against the measured bf16 burst peak. Each of `args.steps` calls sits
     between its own pair of CUDA events on the launching stream after `args.warmup` untimed
-    calls, and a 256 MB write flushes L2 before every call (outside the events)."""
+    calls, and a 256 MB write flushes L2 before every call (outside the events); that time is
+    ms_between_events, and ms is the call's marginal cost in a stream (marginal_ms)."""
     import torch
     from paged_kv_cache_apply_gb300 import device as DV
     from paged_kv_cache_apply_gb300 import workloads as W
@@ -606,18 +653,23 @@ def config_rows(args, peaks, local):
         torch.cuda.synchronize()
         clocks.mark(wall0, time.time())
         clk = clocks.stop()
-        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ms_ev = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        ms = marginal_ms(run, flush, stream, K)
         work = step_work(wl)
-        row = {"op": op, "ms": round(ms, 5), "workload": wl.description, "l2": "flushed before every call",
-               "clocks": clk}
+        row = {"op": op, "ms": round(ms, 5), "ms_between_events": round(ms_ev, 5),
+               "workload": wl.description, "l2": "flushed before every call", "clocks": clk}
         if op == "decode":
             gbs = work["decode_bytes"] / (ms * 1e-3) / 1e9
+            gbs_ev = work["decode_bytes"] / (ms_ev * 1e-3) / 1e9
             row.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                        "frac_hbm_between_events": round(gbs_ev / hbm, 4),
                         "algorithmic_bytes": int(work["decode_bytes"]),
                         "split_chunk": wl.decode.split_chunk})
         else:
             tfs = work["prefill_flops"] / (ms * 1e-3) / 1e12
+            tfs_ev = work["prefill_flops"] / (ms_ev * 1e-3) / 1e12
             row.update({"TFLOP/s": round(tfs, 2), "frac_tc": round(tfs / tc, 4),
+                        "frac_tc_between_events": round(tfs_ev / tc, 4),
                         "algorithmic_flops": int(work["prefill_flops"])})
         out[name] = row
         del dw, wl
