@@ -539,7 +539,8 @@ def run_gpu(args):
                        "main stream, concurrently: the decode with the rope + write of its 256 "
                        "new tokens folded in (astr_decode_attention_rope); the step ends when "
                        "both are done",
-            "timing": "rows: each op's marginal cost in a stream (K pairs of a 256 MB L2 flush "
+            "timing": "rows: each op's marginal cost in a stream (K pairs of an L2 flush (256 MB "
+                      "written, then read) "
                       "and the op between two events, minus K flushes; median of 3), with the "
                       "time between an event on each side of the op as ms_between_events; "
                       "roofline: K steps with the ops serialised and an event between them; "
@@ -585,6 +586,15 @@ def run_gpu(args):
     print(json.dumps(out), flush=True)
 
 
+def flush_l2(buf, i):
+    """Write `buf` (larger than the 129 MB L2), then read it back: L2 then holds only clean
+    lines of `buf`, so the next op reads its inputs from HBM and does not pay for writing the
+    flush's dirty lines back."""
+    import torch
+    buf.fill_(i & 0xFF)
+    buf.view(torch.float32).sum()
+
+
 def marginal_ms(fn, flush, stream, K, rounds=3):
     """The cost of one call of `fn` in a stream of launches: K pairs (an L2 flush, then `fn`)
     between two CUDA events, minus K flushes alone, the median over `rounds` alternations.
@@ -592,7 +602,8 @@ def marginal_ms(fn, flush, stream, K, rounds=3):
     A short kernel timed between its own pair of events also carries the events' cost: on GB300
     an event on each side of a trivial kernel measures 4.4-6 us, most of a 10 us op. Here the
     launches follow one another with no event between them, as in a model's step, and the flush
-    (a 256 MB write, larger than the 129 MB L2) makes every call read its inputs from HBM."""
+    (flush_l2: a 256 MB write and read, larger than the 129 MB L2) makes every call read its
+    inputs from HBM."""
     import torch
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -600,7 +611,7 @@ def marginal_ms(fn, flush, stream, K, rounds=3):
         torch.cuda.synchronize()
         e0.record(stream)
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             if with_fn:
                 fn()
         e1.record(stream)
@@ -621,7 +632,7 @@ def config_rows(args, peaks, local):
     prefill_b8_varlen (varlen causal prefill, half the requests resumed) in TFLOP/s of unmasked
     (query, key) pairs against the measured bf16 burst peak. Each of `args.steps` calls sits
     between its own pair of CUDA events on the launching stream after `args.warmup` untimed
-    calls, and a 256 MB write flushes L2 before every call (outside the events); that time is
+    calls, and a 256 MB write and read flush L2 before every call (outside the events); that time is
     ms_between_events, and ms is the call's marginal cost in a stream (marginal_ms)."""
     import torch
     from paged_kv_cache_apply_gb300 import device as DV
@@ -646,7 +657,7 @@ def config_rows(args, peaks, local):
         clocks.start()
         wall0 = time.time()
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush_l2(flush, i)
             ev[i][0].record(stream)
             run()
             ev[i][1].record(stream)
