@@ -87,6 +87,18 @@ __device__ __forceinline__ void head_bar_sync(int h) {
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
+// O += P V with P (the A operand) read from TMEM, issued by the elected lane of a converged warp
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PreArgs a, const __grid_constant__ CUtensorMap qmap,
@@ -387,57 +399,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (*abort_flag) break;
     }
   } else {
-    // ===================== MMA issuer: lane 0 of warp 9 ========================================
-    // A tcgen05.mma holds its issuing thread for about as long as it occupies the tensor pipe.
-    // One thread issues both heads in a fixed order -- per KV tile, head 0's P.V and next S,
-    // then head 1's -- so each head's MMAs run as a block: head 1's S lands one block after
-    // head 0's, and from then on one head's softmax runs while the tensor core works for the
-    // other, instead of both softmaxes contending for the exp2 unit at once.
-    if (lane == 0) {
-      bool ok = mbar_wait(q_full, 0, a.wait_ns, a.err);
+    // ===================== MMA issuer: warp 9, converged; one elected lane issues ==============
+    // Each head's MMAs run as a block in a fixed order -- per KV tile, head 0's P.V and next S,
+    // then head 1's -- so head 1's S lands one block after head 0's, and from then on one
+    // head's softmax runs while the tensor core works for the other. Descriptors are built once
+    // per buffer and stepped by constants (16-byte units); the whole warp runs the loop and an
+    // elected lane issues, which keeps the issue at the tensor core's rate (a loop run by one
+    // lane of a divergent branch with two descriptors built per MMA measured about 120 cycles an
+    // issue against the tensor core's 64).
+    {
       auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
-        if (*abort_flag || !mbar_wait(bar, parity, a.wait_ns, a.err)) return false;
-        tc::fence_after_sync();
-        tc::fence_proxy_async_smem();  // rows that came by cp.async (generic proxy)
-        return true;
+        bool got = !*abort_flag && mbar_wait_sleep(bar, parity, a.wait_ns, a.err);
+        got = __all_sync(0xffffffffu, got);
+        if (got) {
+          tc::fence_after_sync();
+          tc::fence_proxy_async_smem();  // rows that came by cp.async (generic proxy)
+        }
+        return got;
       };
+      constexpr uint64_t kStep = kTile >> 4;
+      const uint64_t q_desc = tc::desc_sw128(sbase + kOffQ, 16, 1024);     // head 0's Q
+      const uint64_t k_desc = tc::desc_sw128(sbase + kOffK, 16, 1024);     // K stage 0
+      const uint64_t v_desc = tc::desc_sw128(sbase + kOffV, kBlk, 1024);   // V stage 0, MN-major
       auto qk = [&](int hh, int j) {
-        const uint32_t qaddr = sbase + kOffQ + hh * kTile;
-        const uint32_t kaddr = sbase + kOffK + (j & 1) * kTile;
+        const uint64_t qd = q_desc + (uint64_t)hh * kStep;
+        const uint64_t kd = k_desc + (uint64_t)(j & 1) * kStep;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint64_t ad = tc::desc_sw128(qaddr + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::desc_sw128(kaddr + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024);
-          tc::mma_ss(tmem + hh * 128, ad, bd, kIdescQK, ks > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)((ks >> 2) * (kBlk >> 4) + (ks & 3) * 2);  // 16-element step
+          tc::mma_ss_elect(tmem + hh * 128, qd + off, kd + off, kIdescQK, ks > 0 ? 1u : 0u);
         }
-        tc::mma_commit(&s_full[hh]);
+        tc::mma_commit_elect(&s_full[hh]);
       };
+      bool ok = __all_sync(0xffffffffu, mbar_wait_sleep(q_full, 0, a.wait_ns, a.err));
       if (ok) {
         tc::fence_after_sync();
         ok = wait(&k_full[0], 0);
         if (ok) {
           for (int hh = 0; hh < NQ; ++hh) qk(hh, 0);
-          tc::mma_commit(&k_empty[0]);
+          tc::mma_commit_elect(&k_empty[0]);
         }
         for (int j = 0; j < nkv && ok; ++j) {
           if (!wait(&v_full[j & 1], (j >> 1) & 1)) {
             ok = false;
             break;
           }
-          const uint32_t vaddr = sbase + kOffV + (j & 1) * kTile;
+          const uint64_t vd = v_desc + (uint64_t)(j & 1) * kStep;
           for (int hh = 0; hh < NQ && ok; ++hh) {
             if (!wait(&p_full[hh], j & 1)) {
               ok = false;
               break;
             }
 #pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks) {
-              const uint64_t bd = tc::desc_sw128(vaddr + ks * 2048, kBlk, 1024);
-              tc::mma_ts(tmem + 256 + hh * 128, tmem + hh * 128 + ks * 8, bd, kIdescPV,
-                         (j > 0 || ks > 0) ? 1u : 0u);
-            }
+            for (int ks = 0; ks < kKeys / 16; ++ks)
+              mma_ts_elect(tmem + 256 + hh * 128, tmem + hh * 128 + ks * 8, vd + (uint64_t)ks * (2048 >> 4),
+                           kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
             if (j + 1 == nkv) {
-              tc::mma_commit(&o_done[hh]);
+              tc::mma_commit_elect(&o_done[hh]);
             } else {
               if (hh == 0 && !wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
                 ok = false;
@@ -447,15 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          tc::mma_commit(&v_empty[j & 1]);
-          if (j + 1 < nkv) tc::mma_commit(&k_empty[(j + 1) & 1]);
+          tc::mma_commit_elect(&v_empty[j & 1]);
+          if (j + 1 < nkv) tc::mma_commit_elect(&k_empty[(j + 1) & 1]);
         }
       }
       if (!ok) *abort_flag = 1;
-      tc::mma_commit(drain);
-      mbar_wait(drain, 0, kDrainLimitNs, a.err);
+      tc::mma_commit_elect(drain);  // nothing may still be in flight when TMEM is freed
+      mbar_wait_sleep(drain, 0, kDrainLimitNs, a.err);
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   tc::fence_before_sync();
