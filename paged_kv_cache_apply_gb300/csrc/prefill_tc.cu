@@ -131,16 +131,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = (int)(blockIdx.x % pairs) * NQ;
   const int G = a.H / a.Hk;
   const int g = h0 / G;
+  // The item's metadata in two rounds of loads: the tile's entries, then the request's lengths
+  // and page-table row together (read at a clamped index, checked afterwards), since each round
+  // costs a memory latency before anything else can start.
   const int b = __ldg(a.tile_b + tile);
+  const int ti = __ldg(a.tile_i + tile);
+  const int bc = b < 0 ? 0 : (b >= a.B ? a.B - 1 : b);
+  const int32_t qo_a = __ldg(a.qo_indptr + bc), qo_b = __ldg(a.qo_indptr + bc + 1);
+  const int32_t kv_a = __ldg(a.kv_indptr + bc), kv_b = __ldg(a.kv_indptr + bc + 1);
+  const int rq = __ldg(a.rpi + bc);
   if (b == -1) return;  // an empty entry of the tile list
   if (b < 0 || b >= a.B) {
     if (tid == 0) raise_error(a.err, ASTR_DEVERR_META);
     return;
   }
-  const int ti = __ldg(a.tile_i + tile);
-  const int64_t q0 = __ldg(a.qo_indptr + b);
-  const int64_t Qb = (int64_t)__ldg(a.qo_indptr + b + 1) - q0;
-  const int64_t Kb = (int64_t)__ldg(a.kv_indptr + b + 1) - __ldg(a.kv_indptr + b);
+  const int64_t q0 = qo_a;
+  const int64_t Qb = (int64_t)qo_b - q0;
+  const int64_t Kb = (int64_t)kv_b - kv_a;
   const int64_t Pb = Kb - Qb;
   const int64_t r0 = (int64_t)ti * kRows;  // first request-local row of the tile
   if (ti < 0 || r0 >= Qb) {
@@ -151,7 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) raise_error(a.err, ASTR_DEVERR_LEN);
     return;
   }
-  const int rq = __ldg(a.rpi + b);
   if (rq < 0 || rq >= a.num_reqs) {
     if (tid == 0) raise_error(a.err, ASTR_DEVERR_ROW);
     return;
