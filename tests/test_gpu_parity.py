@@ -403,3 +403,23 @@ def test_decode_large_batches_rank_or_not(B, lens_kind):
     # and no request was skipped: every output row was written (zeroed before the call)
     assert np.all(np.any(got.reshape(B, -1) != 0, axis=1))
     assert A.astr_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype,H,Hk,D", [
+    ("bf16", 24, 4, 128),   # 32 head rows x 16 chunks = 512 chunks: four per thread of a 128-thread block
+    ("bf16", 32, 4, 128),   # 640 chunks: more than four per thread, the one-thread-per-chunk kernel
+    ("f32", 40, 8, 128),    # 896 chunks of 32 bytes
+    ("bf16", 2, 1, 64),     # 32 chunks: one per thread, most threads idle
+])
+def test_rope_write_chunks_per_thread(dtype, H, Hk, D):
+    """The rotate + write over every chunk-per-thread count the block-per-token launch takes,
+    bit for bit against the oracle (q_out, and the whole layer of both caches)."""
+    wl = W.make_case(dtype, H, Hk, D, 16, [5, 130, 257], [5, 130, 257], with_rope=True,
+                     seed=W.SEED_BASE + 700 + H + Hk + D)
+    dw = DV.DeviceWorkload.upload(wl)
+    kl, vl = host_layer(wl, 1)
+    dw.run_rope()
+    _sync()
+    check_rope(dw, "rope", kl, vl)
+    check_cache_equal(dw, 1, kl, vl)
+    assert A.astr_device_error() == 0
