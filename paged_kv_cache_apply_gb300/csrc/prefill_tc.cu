@@ -14,10 +14,11 @@
 //    box per run of 16 keys whose slots are consecutive (a page; destinations 2 KB aligned),
 //    16-byte cp.async copies for keys outside such runs, zero-filled past the request; the
 //    page-table entries of a tile are read while the previous tile's copies are issued;
-//  * warp 9 allocates all 512 TMEM columns -- S0 | S1 | O0 | O1, 128 each -- and one of its
-//    threads issues the MMAs, S_h = Q_h K^T (M = N = K = 128) and O_h += P_h V (P_h read
-//    from TMEM where the softmax wrote it over S_h, V an MN-major operand), head by head, so
-//    that the tensor core works on one head while the other head's softmax runs;
+//  * warp 9 allocates all 512 TMEM columns -- S0 | S1 | O0 | O1, 128 each -- and issues the
+//    MMAs (the whole warp runs converged, an elected lane issues, descriptors are built once
+//    per buffer), S_h = Q_h K^T (M = N = K = 128) and O_h += P_h V (P_h read from TMEM where
+//    the softmax wrote it over S_h, V an MN-major operand), head by head, so that the tensor
+//    core works on one head while the other head's softmax runs;
 //  * warps 0-3 and 4-7 are the softmax of head 0 and head 1, one thread per row holding all
 //    128 scores of a tile in registers: the row max, the reference max raised only when the
 //    row max exceeds it by 2^8 (the O row is then rescaled in TMEM; the commit that published
