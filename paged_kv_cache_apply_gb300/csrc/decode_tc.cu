@@ -17,8 +17,9 @@
 //  * warps 4-7 stream 128-token tiles of the item's KV-head slices of K and V into a 3-stage
 //    ring in the 128-byte-swizzled operand layout, 32 tokens per warp: when those are two
 //    whole pages (two runs of 16 consecutive slots) they come as four TMA boxes of 16 rows
-//    (one per 64-element half of K and of V), otherwise as 16-byte cp.async copies (two
-//    lane-halves per token row, fully coalesced) with positions past the chunk zero-filled.
+//    (one per 64-element half of K and of V), otherwise as 16-byte cp.async copies (eight
+//    lanes per token row, four whole rows per instruction; the lanes take their rows' slots
+//    from shared memory) with positions past the chunk zero-filled.
 //    Which path a warp takes is uniform across it, so the copy loop stays straight-line code;
 //  * warp 8 allocates 64 TMEM columns -- two S buffers and two O^T buffers of 16 columns --
 //    and issues, per tile, S^T = K Q^T (M = 128 tokens on the TMEM lanes, N = 16 query rows
@@ -71,7 +72,8 @@ constexpr int kOffMisc = kOffRing + 2 * 64;
 constexpr int kSortMax = 1024;                        // batches up to this size claim longest first
 constexpr int kBuckets = 1024;                        // seq_len ranks by 128-token tile count
 constexpr int kOffOrder = kOffMisc + 64;              // [kSortMax] requests by seq_len, [kBuckets] counts
-constexpr int kSmemBytes = kOffOrder + (kSortMax + kBuckets) * 4 + 1024;  // + alignment slack
+constexpr int kOffSlots = kOffOrder + (kSortMax + kBuckets) * 4;  // [4 loader warps][2][32] slots
+constexpr int kSmemBytes = kOffSlots + 4 * 2 * 32 * 4 + 1024;  // + alignment slack
 
 constexpr uint32_t kIdescQK = tc::idesc_bf16(128, kNPad, false, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, kNPad, true, false);
@@ -548,18 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           // Eight lanes per token row, two 16-byte chunks each (c8 and c8 + 8, one in each
-          // 64-element half): four whole rows per copy instruction. The slots of this lane's
-          // eight rows (checked above to lie in [0, size) or be -1; they come from int32
-          // page-table entries) are all gathered before any copy, so the 32 copies issue back
-          // to back. Measured on GB300 against one chunk of 16 rows per lane (16 slots to
-          // gather): one-token pages 77.4 against 79.7 us; four lanes per row with four chunks
-          // each (eight half rows per instruction) took 85.1 us.
-          int32_t sl[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) sl[jj] = __shfl_sync(0xffffffffu, (int32_t)my, jj * 4 + q4);
+          // 64-element half): four whole rows per copy instruction. Lanes 8q .. 8q + 7 copy the
+          // rows of tokens 8q .. 8q + 7 of the warp's 32, whose slots (checked above to lie in
+          // [0, size) or be -1) they read back from shared memory as two 16-byte vectors; the
+          // buffer alternates by tile, so one warp barrier orders each tile's writes and reads.
+          // Measured on GB300 (one-token pages): 76.1 us, against 77.4 with the slots gathered
+          // by eight shuffles, 79.7 with one chunk of 16 rows per lane (16 shuffles) and 85.1
+          // with four lanes per row.
+          int32_t *sx = reinterpret_cast<int32_t *>(smem + kOffSlots) + lw * 64 + (it & 1) * 32;
+          sx[lane] = (int32_t)my;
+          __syncwarp();
+          const int4 s0 = *reinterpret_cast<const int4 *>(sx + q4 * 8);
+          const int4 s1 = *reinterpret_cast<const int4 *>(sx + q4 * 8 + 4);
+          const int32_t sl[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const int t = lw * 32 + jj * 4 + q4;  // token within the tile
+            const int t = lw * 32 + q4 * 8 + jj;  // token within the tile
             const uint32_t off = tc::sw128_chunk_offset(t, c8, kBlockBytes);
             const bool v = sl[jj] >= 0;
             const int64_t go = v ? (int64_t)sl[jj] * rowb + c8 * 16 : 0;
