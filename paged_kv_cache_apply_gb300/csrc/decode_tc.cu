@@ -27,7 +27,8 @@
 //    head_dim, N = 16, K = 128 tokens) with V read as an MN-major operand and P^T from shared
 //    memory; consecutive items accumulate into alternate O^T buffers;
 //  * warps 0-3 (one TMEM lane each) read a token's G scores, take the tile max per head
-//    across the 128 lanes (warp shuffles + one named barrier), keep the softmax reference
+//    across the 128 lanes (a butterfly of warp shuffles that splits the G values across
+//    lanes, then one named barrier), keep the softmax reference
 //    max lazily (raised only when a score exceeds it by 2^8, then O^T is rescaled in TMEM),
 //    write P^T in bf16 and, after an item's last tile, normalise O^T and store the output or
 //    the chunk's partial and (m, l).
@@ -362,13 +363,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           ld_cols<G>(tS0 + lane_base + sb * 16, s);
           const bool valid = tid < nv;
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            x[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
-            float wmax = x[h];
+          for (int h = 0; h < G; ++h) x[h] = valid ? s[h] * a.scale_log2 : -INFINITY;
+          // The warp's G maxima in (G - 1) + 5 - log2(G) shuffles instead of 5 G: while a lane
+          // holds w > 1 values, the exchange across lane bit m halves them (a lane with the bit
+          // set keeps the upper half and sends the lower one), and single values then finish
+          // the remaining lane bits. The lanes whose low log2(32 / G) bits are zero end with one
+          // head's maximum each (head hsel). Measured on GB300 against five shuffles per head
+          // (G = 4): one-token pages 75.8 against 76.4 us, the mixed batch 328.1 against 329.2.
+          float v[G];
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-            if (lane == 0) red[(sb * 4 + warp) * 16 + h] = wmax;
+          for (int h = 0; h < G; ++h) v[h] = x[h];
+          int hsel = 0;
+#pragma unroll
+          for (int w = G, m = 16; w > 1; w >>= 1, m >>= 1) {
+            const bool up = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < w / 2; ++i) {
+              const float send = up ? v[i] : v[i + w / 2];
+              const float keep = up ? v[i + w / 2] : v[i];
+              v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, m));
+            }
+            if (up) hsel += w / 2;
           }
+#pragma unroll
+          for (int m = 16 / G; m >= 1; m >>= 1) v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], m));
+          if ((lane & (32 / G - 1)) == 0) red[(sb * 4 + warp) * 16 + hsel] = v[0];
         }
         if (bar_any(1, 128, !ok)) {
           aborted = true;
