@@ -395,12 +395,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mnew[G];
         bool changed = false;
+        float M[G];
+        // the four warps' maxima, read as 16-byte vectors where G allows (measured on GB300 with the
+        // row sums' butterfly below: one-token pages 75.8 against 76.8 us)
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int h4 = 0; h4 < G; h4 += 4) {
+              const float4 r4 = *reinterpret_cast<const float4 *>(red + (sb * 4 + q) * 16 + h4);
+              M[h4 + 0] = q == 0 ? r4.x : fmaxf(M[h4 + 0], r4.x);
+              M[h4 + 1] = q == 0 ? r4.y : fmaxf(M[h4 + 1], r4.y);
+              M[h4 + 2] = q == 0 ? r4.z : fmaxf(M[h4 + 2], r4.z);
+              M[h4 + 3] = q == 0 ? r4.w : fmaxf(M[h4 + 3], r4.w);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            M[h] = red[(sb * 4 + 0) * 16 + h];
+#pragma unroll
+            for (int q = 1; q < 4; ++q) M[h] = fmaxf(M[h], red[(sb * 4 + q) * 16 + h]);
+          }
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float M = red[(sb * 4 + 0) * 16 + h];
-#pragma unroll
-          for (int q = 1; q < 4; ++q) M = fmaxf(M, red[(sb * 4 + q) * 16 + h]);
-          mnew[h] = (M > m[h] + kLazyRescale) ? M : m[h];
+          mnew[h] = (M[h] > m[h] + kLazyRescale) ? M[h] : m[h];
           changed |= mnew[h] != m[h];
         }
         if (changed) {  // the same decision in every thread
@@ -449,12 +469,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
+      {  // l over the 128 token lanes: the value-splitting butterfly of the tile maxima, with sums
+        float v[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {  // l over the 128 token lanes
-        float v = l[h];
+        for (int h = 0; h < G; ++h) v[h] = l[h];
+        int hsel = 0;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) lsum_s[warp * 16 + h] = v;
+        for (int w = G, m = 16; w > 1; w >>= 1, m >>= 1) {
+          const bool up = (lane & m) != 0;
+#pragma unroll
+          for (int i = 0; i < w / 2; ++i) {
+            const float send = up ? v[i] : v[i + w / 2];
+            const float keep = up ? v[i + w / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+          if (up) hsel += w / 2;
+        }
+#pragma unroll
+        for (int m = 16 / G; m >= 1; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+        if ((lane & (32 / G - 1)) == 0) lsum_s[warp * 16 + hsel] = v[0];
       }
       bar_sync(1, 128);
       float o[G];
